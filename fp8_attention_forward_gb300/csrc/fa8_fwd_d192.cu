@@ -1,0 +1,6 @@
+// Instantiations of the forward kernel for (d, dv) = (192, 128) and (192, 192).
+#include "fa8_launch.h"
+namespace fa8 {
+FA8_DEFINE_FWD(192, 128)
+FA8_DEFINE_FWD(192, 192)
+}  // namespace fa8

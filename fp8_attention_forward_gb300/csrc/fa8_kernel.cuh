@@ -1,0 +1,787 @@
+// fa8_kernel.cuh -- the fused FP8 attention forward for sm_103a (tcgen05 + TMA + TMEM)
+// and the split-KV combine kernel.
+//
+// One CTA computes one 128-row Q tile: the rows are (query position, q-head) pairs of one
+// kv-head group, packed position-major (PackGQA), against the kv-head's keys, for one
+// split of the request's key range.  Roles (320 threads):
+//   warps 0-3  softmax: thread r owns TMEM lane r = tile row r
+//   warps 4-7  correction: two-level PV fold into fp32 O, epilogue
+//   warp 8     TMA producer (Q once, K/V tiles into S-stage rings)
+//   warp 9     MMA issuer (lane 0) and TMEM owner
+//
+// Per 128-key tile t (sources: "[Cute,Fwd,Sm90] Native FP8 (E4M3 Q/K/V) forward for
+// Hopper", Design; "tml-fa4 PR #4", Summary and "Correctness fix over #1"):
+//   S_t   = Q K_t^T                     tcgen05.mma kind::f8f6f4, fp32 in TMEM
+//   m     lazy running max: moved only when the tile max exceeds it by more than
+//         tau = 0.75 (log2 units), tau <= log2(448) - 8 so that P never clips
+//   P_t   = 2^(s*c - m + 8) -> E4M3 (c = softmax_scale * dq * dk * log2 e), stored
+//         in TMEM over the first 32 columns of S_t
+//   O_t   = P_t V_t                     accumulated from zero for every tile
+//   O     = O * alpha + O_t             fp32 fold (two-level accumulation)
+// and after the last tile O * dv / rowsum -> bf16/fp16, LSE = ln2*(log2 rowsum + m - 8).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "fa8_ptx.cuh"
+
+namespace fa8 {
+
+constexpr int kTileM = 128;     // Q rows per CTA = TMEM lanes
+constexpr int kTileN = 128;     // keys per KV tile
+constexpr int kNumThreads = 320;
+constexpr float kTau = 0.75f;   // lazy-rescale threshold, log2 units
+constexpr float kPBias = 8.0f;  // P carries a factor 2^8
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+enum : unsigned { kStatusTimeout = 1u, kStatusBounds = 2u };
+
+struct FwdParams {
+    int B, Hq, Hkv, G, rows_per_tile, pos_per_tile;
+    int q_varlen;  // q is (total_q, Hq, D) with cu_q
+    int kv_mode;   // 0 batched, 1 varlen, 2 paged
+    int Sq, Sk;    // batched lengths
+    int total_q, total_k;
+    int mblocks_per_batch;  // batched Q: ceil(Sq / pos_per_tile)
+    const int *cu_q;
+    const int *cu_k;
+    const int *block_table;
+    long long bt_stride;
+    int max_pages, page_size, box_n, boxes_per_tile, num_pages;
+    const float *dq, *dk, *dv;
+    long long dq_sb, dq_sh, dk_sb, dk_sh, dv_sb, dv_sh;
+    const float *sink;
+    float scale_log2;  // softmax_scale * log2(e)
+    int causal, window_left;
+    int num_splits;
+    int split_mode;  // write fp32 partials for the combine kernel
+    void *o;
+    long long o_sb, o_ss, o_sh;
+    int out_fp16;
+    float *lse;
+    long long lse_sb, lse_sh, lse_ss;
+    float *o_part, *lse_part;
+    unsigned long long timeout_ns;
+    unsigned int *status;
+};
+
+struct CombineParams {
+    int total_q, Hq, num_splits, q_varlen, Sq;
+    const float *o_part, *lse_part;
+    void *o;
+    long long o_sb, o_ss, o_sh;
+    int out_fp16;
+    float *lse;
+    long long lse_sb, lse_sh, lse_ss;
+};
+
+// Compile-time tile configuration for head dims (D, DV).
+template <int D, int DV>
+struct Cfg {
+    // Q/K rows are split along D into chunks of CW bytes, each its own swizzled block.
+    static constexpr int CW = (D % 128 == 0) ? 128 : ((D % 64 == 0) ? 64 : 32);
+    static constexpr int NCK = D / CW;
+    // V rows are split along DV into chunks of CWV bytes (MN-major operand of PV).
+    static constexpr int CWV = (DV % 128 == 0) ? 128 : ((DV % 64 == 0) ? 64 : 32);
+    static constexpr int NCV = DV / CWV;
+    // Running O lives in registers when it fits (dv <= 128), else in TMEM.
+    static constexpr bool O_REGS = DV <= 128;
+    static constexpr int NS = O_REGS ? 2 : 1;  // S/P buffers in TMEM
+    static constexpr int OTW = (NS * 128 + DV + (O_REGS ? 0 : DV) <= 512) ? DV : DV / 2;
+    static constexpr int NPV = DV / OTW;  // PV MMAs per tile (dv split through one O_tile)
+    static constexpr uint32_t TM_S = 0;
+    static constexpr uint32_t TM_OT = NS * 128;
+    static constexpr uint32_t TM_OR = TM_OT + OTW;
+    static constexpr uint32_t TM_COLS = 512;
+    static constexpr int CHUNK_Q = kTileM * CW;
+    static constexpr int CHUNK_K = kTileN * CW;
+    static constexpr int CHUNK_V = kTileN * CWV;
+    static constexpr int Q_BYTES = kTileM * D;
+    static constexpr int K_BYTES = kTileN * D;
+    static constexpr int V_BYTES = kTileN * DV;
+    static constexpr int MISC_BYTES = 4096;
+    static constexpr int SMEM_LIMIT = 232448;  // max dynamic smem per block on sm_103
+    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - MISC_BYTES - Q_BYTES) / (K_BYTES + V_BYTES);
+    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = Q_BYTES;
+    static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
+    static constexpr int OFF_MISC = OFF_V + STAGES * V_BYTES;
+    static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
+    // barrier slots
+    static constexpr int B_Q = 0;
+    static constexpr int B_KF = 1;
+    static constexpr int B_KE = B_KF + STAGES;
+    static constexpr int B_VF = B_KE + STAGES;
+    static constexpr int B_VE = B_VF + STAGES;
+    static constexpr int B_SF = B_VE + STAGES;
+    static constexpr int B_PF = B_SF + NS;
+    static constexpr int B_OF = B_PF + NS;
+    static constexpr int B_OE = B_OF + 1;
+    static constexpr int B_AF = B_OE + 1;  // 2 slots
+    static constexpr int B_AE = B_AF + 2;  // 2 slots
+    static constexpr int B_DONE = B_AE + 2;
+    static constexpr int NUM_BARS = B_DONE + 1;
+    static_assert(STAGES >= 2, "smem too small for two K/V stages");
+    static_assert(NUM_BARS * 8 <= 512, "barrier area");
+    static_assert(TM_OR + (O_REGS ? 0 : DV) <= TM_COLS, "TMEM budget");
+    static_assert(OTW % CWV == 0 && OTW % 32 == 0 && OTW % 16 == 0 && OTW <= 256, "PV shape");
+    static_assert(D % 32 == 0 && DV % 32 == 0, "head dims");
+};
+
+// UMMA shared-memory descriptor: start >>4 [0,14), LBO >>4 [16,30), SBO >>4 [32,46),
+// fixed 0b001 at [46,49), swizzle layout at [61,64) (2 = 128B, 4 = 64B, 6 = 32B).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                          uint32_t layout) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)layout << 61;
+    return d;
+}
+__host__ __device__ constexpr uint32_t swz_layout(int chunk_bytes) {
+    return chunk_bytes == 128 ? 2u : (chunk_bytes == 64 ? 4u : 6u);
+}
+// Instruction descriptor, kind::f8f6f4: D fp32 (bit 4), A/B E4M3 (0), B major at bit 16,
+// N>>3 at [17,23), M>>4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// Bounded mbarrier waits: give up when another role aborted or after timeout_ns, setting
+// the CTA abort flag and the device status word.
+struct Waiter {
+    volatile int *abort;
+    unsigned long long timeout;
+    unsigned int *status;
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = ptx::globaltimer();
+        while (true) {
+#pragma unroll 1
+            for (int i = 0; i < 32; ++i)
+                if (ptx::mbar_try_wait(bar, parity)) return true;
+            if (*abort) return false;
+            if (ptx::globaltimer() - t0 > timeout) {
+                *abort = 1;
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+    // Used when draining in-flight async work before exit: ignores the abort flag.
+    __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(bar, parity)) {
+            if (ptx::globaltimer() - t0 > timeout) {
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
+        }
+        return true;
+    }
+};
+
+// Maps a varlen grid slot to (request, m-block): the slots enumerate each request's
+// m-blocks in order; within a request the m-block order is reversed so that, with a
+// causal mask, the longer rows start first.  Whole warp must call it.
+__device__ __forceinline__ bool varlen_slot(const FwdParams &p, int x, int &b, int &mb) {
+    const int lane = threadIdx.x & 31;
+    const int P = p.pos_per_tile;
+    int base = 0;
+    for (int s0 = 0; s0 < p.B; s0 += 32) {
+        const int s = s0 + lane;
+        int cnt = 0;
+        if (s < p.B) {
+            const int len = p.cu_q[s + 1] - p.cu_q[s];
+            cnt = len > 0 ? (len + P - 1) / P : 0;
+        }
+        int inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        const int cum = base + inc;
+        const unsigned m = __ballot_sync(0xffffffffu, s < p.B && x < cum);
+        if (m) {
+            const int l = __ffs(m) - 1;
+            const int ci = __shfl_sync(0xffffffffu, cum, l);
+            const int cn = __shfl_sync(0xffffffffu, cnt, l);
+            b = s0 + l;
+            mb = cn - 1 - (x - (ci - cn));
+            return true;
+        }
+        base += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    return false;
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// Writes 8 consecutive output values (one 16-byte store) in bf16 or fp16.
+__device__ __forceinline__ void store8(void *dst, const float *v, int fp16) {
+    uint4 pk;
+    uint32_t *w = reinterpret_cast<uint32_t *>(&pk);
+    if (fp16) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+    }
+    *reinterpret_cast<uint4 *>(dst) = pk;
+}
+
+template <int D, int DV>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
+               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+    using C = Cfg<D, DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    // ------------------------------------------------------------ tile schedule
+    int b, mb;
+    if (!p.q_varlen) {
+        const int x = blockIdx.x;
+        b = x % p.B;
+        mb = p.mblocks_per_batch - 1 - x / p.B;
+    } else if (!varlen_slot(p, blockIdx.x, b, mb)) {
+        return;  // slot beyond the last request's m-blocks
+    }
+    const int kvh = blockIdx.y % p.Hkv;
+    const int split = blockIdx.y / p.Hkv;
+    const int P = p.pos_per_tile;
+    const int q_start = p.q_varlen ? p.cu_q[b] : b * p.Sq;
+    int Lq = p.q_varlen ? p.cu_q[b + 1] - q_start : p.Sq;
+    int Lk, k_start = 0;
+    if (p.kv_mode == 0) {
+        Lk = p.Sk;
+    } else {
+        k_start = p.cu_k[b];
+        Lk = p.cu_k[b + 1] - k_start;
+    }
+    // device-side sanity of caller-provided lengths: never index outside the tensors
+    bool bad = Lq < 0 || Lk < 0 || q_start < 0 || q_start + Lq > p.total_q;
+    if (p.kv_mode == 1) bad |= (k_start < 0 || k_start + Lk > p.total_k);
+    if (p.kv_mode == 2) bad |= ((long long)Lk > (long long)p.max_pages * p.page_size);
+    if (bad) {
+        if (tid == 0) atomicOr(p.status, kStatusBounds);
+        return;
+    }
+    const int pos0 = mb * P;
+    if (pos0 >= Lq) return;
+    const int pos_last = min(pos0 + P, Lq) - 1;
+    const int delta = Lk - Lq;
+    const int kv_end = p.causal ? min(Lk, pos_last + delta + 1) : Lk;
+    const int kv_beg = p.window_left >= 0 ? max(0, pos0 + delta - p.window_left) : 0;
+    int t_beg = 0, n_tiles = 0;
+    if (kv_end > kv_beg) {
+        const int tb = kv_beg / kTileN;
+        const int te = (kv_end + kTileN - 1) / kTileN;
+        const int per = (te - tb + p.num_splits - 1) / p.num_splits;
+        t_beg = tb + split * per;
+        n_tiles = max(0, min(te, t_beg + per) - t_beg);
+    }
+
+    // ------------------------------------------------------------ per-row facts
+    const int r = tid & 127;  // tile row of softmax / correction threads
+    const int rpos = pos0 + r / p.G;
+    const int hq = kvh * p.G + r % p.G;
+    const bool row_ok = r < p.rows_per_tile && rpos < Lq;
+    const int tok = q_start + rpos;  // packed query token index
+    const long long beta = p.q_varlen ? 0 : b;
+    const long long rho = p.q_varlen ? tok : rpos;
+    const bool has_sink = p.sink != nullptr && (!p.split_mode || split == 0);
+
+    if (n_tiles == 0) {
+        // nothing visible for this CTA: O = 0, LSE = -inf (or the sink logit)
+        if (tid < 128 && row_ok) {
+            const float lse = has_sink ? p.sink[hq] : -INFINITY;
+            if (p.split_mode) {
+                const long long row = ((long long)split * p.total_q + tok) * p.Hq + hq;
+                p.lse_part[row] = lse;
+                float4 *dst = reinterpret_cast<float4 *>(p.o_part + row * DV);
+                for (int i = 0; i < DV / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                if (p.lse) p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
+                uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) +
+                               2 * (beta * p.o_sb + rho * p.o_ss + hq * p.o_sh);
+                for (int i = 0; i < DV / 8; ++i)
+                    *reinterpret_cast<uint4 *>(dst + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ shared memory
+    uint8_t *misc = smem + C::OFF_MISC;
+    const uint32_t bar0 = ptx::smem_u32(misc);
+    auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc + 512);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 516);
+    float *alpha_ring = reinterpret_cast<float *>(misc + 1024);  // [2][128]
+    float *row_scale = reinterpret_cast<float *>(misc + 2048);   // [128]
+    const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
+    const uint32_t sK = ptx::smem_u32(smem + C::OFF_K);
+    const uint32_t sV = ptx::smem_u32(smem + C::OFF_V);
+
+    if (tid == 0) {
+        ptx::mbar_init(BAR(C::B_Q), 1);
+        for (int i = 0; i < C::STAGES; ++i) {
+            ptx::mbar_init(BAR(C::B_KF + i), 1);
+            ptx::mbar_init(BAR(C::B_KE + i), 1);
+            ptx::mbar_init(BAR(C::B_VF + i), 1);
+            ptx::mbar_init(BAR(C::B_VE + i), 1);
+        }
+        for (int i = 0; i < C::NS; ++i) {
+            ptx::mbar_init(BAR(C::B_SF + i), 1);
+            ptx::mbar_init(BAR(C::B_PF + i), 128);
+        }
+        ptx::mbar_init(BAR(C::B_OF), 1);
+        ptx::mbar_init(BAR(C::B_OE), 128);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(BAR(C::B_AF + i), 128);
+            ptx::mbar_init(BAR(C::B_AE + i), 128);
+        }
+        ptx::mbar_init(BAR(C::B_DONE), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == 8 && lane == 0) {
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+    }
+    if (warp == 9) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Waiter W{abort_flag, p.timeout_ns, p.status};
+
+    if (warp == 8) {
+        // ======================================================== TMA producer
+        const bool paged = p.kv_mode == 2;
+        int issued_k = 0, issued_v = 0;
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(BAR(C::B_Q), (uint32_t)(D * p.rows_per_tile));
+            const int c2 = p.q_varlen ? q_start + pos0 : pos0;
+            const int c3 = p.q_varlen ? 0 : b;
+#pragma unroll
+            for (int c = 0; c < C::NCK; ++c)
+                ptx::tma_load_4d(sQ + c * C::CHUNK_Q, &tm_q, BAR(C::B_Q), c * C::CW, kvh * p.G, c2, c3);
+        }
+        for (int it = 0; it < n_tiles; ++it) {
+            const int k0 = (t_beg + it) * kTileN;
+            const int st = it % C::STAGES;
+            const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+            // paged: lane i looks up the page of box i of this tile
+            int page = 0, prow = 0;
+            if (paged && lane < p.boxes_per_tile) {
+                const int j0 = k0 + lane * p.box_n;
+                const int pi = j0 / p.page_size;
+                prow = j0 - pi * p.page_size;
+                page = p.num_pages;  // past the request's keys: out of range, TMA fills zeros
+                if (j0 < Lk) {
+                    const int e = p.block_table[(long long)b * p.bt_stride + pi];
+                    if (e >= 0 && e < p.num_pages) page = e;
+                    else atomicOr(p.status, kStatusBounds);
+                }
+            }
+            const int c2 = p.kv_mode == 1 ? k_start + k0 : k0;
+            const int c3 = p.kv_mode == 1 ? 0 : b;
+            // K tile
+            if (!W.wait(BAR(C::B_KE + st), ph ^ 1u)) break;
+            if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_KF + st), (uint32_t)C::K_BYTES);
+            __syncwarp();
+            const uint32_t dK = sK + st * C::K_BYTES;
+            if (paged) {
+                if (lane < p.boxes_per_tile) {
+#pragma unroll
+                    for (int c = 0; c < C::NCK; ++c)
+                        ptx::tma_load_4d(dK + c * C::CHUNK_K + lane * p.box_n * C::CW, &tm_k,
+                                         BAR(C::B_KF + st), c * C::CW, kvh, prow, page);
+                }
+            } else if (lane == 0) {
+#pragma unroll
+                for (int c = 0; c < C::NCK; ++c)
+                    ptx::tma_load_4d(dK + c * C::CHUNK_K, &tm_k, BAR(C::B_KF + st), c * C::CW, kvh, c2, c3);
+            }
+            issued_k = it + 1;
+            // V tile
+            if (!W.wait(BAR(C::B_VE + st), ph ^ 1u)) break;
+            if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_VF + st), (uint32_t)C::V_BYTES);
+            __syncwarp();
+            const uint32_t dV = sV + st * C::V_BYTES;
+            if (paged) {
+                if (lane < p.boxes_per_tile) {
+#pragma unroll
+                    for (int c = 0; c < C::NCV; ++c)
+                        ptx::tma_load_4d(dV + c * C::CHUNK_V + lane * p.box_n * C::CWV, &tm_v,
+                                         BAR(C::B_VF + st), c * C::CWV, kvh, prow, page);
+                }
+            } else if (lane == 0) {
+#pragma unroll
+                for (int c = 0; c < C::NCV; ++c)
+                    ptx::tma_load_4d(dV + c * C::CHUNK_V, &tm_v, BAR(C::B_VF + st), c * C::CWV, kvh, c2, c3);
+            }
+            issued_v = it + 1;
+        }
+        if (*abort_flag) {
+            // every load already issued must land before the CTA's smem is released;
+            // the newest load of each ring slot is the one that can still be in flight
+            W.drain(BAR(C::B_Q), 0);
+            for (int i = max(0, issued_k - C::STAGES); i < issued_k; ++i)
+                W.drain(BAR(C::B_KF + i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u);
+            for (int i = max(0, issued_v - C::STAGES); i < issued_v; ++i)
+                W.drain(BAR(C::B_VF + i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ======================================================== MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescQK = idesc_e4m3(kTileM, kTileN, false);
+            constexpr uint32_t kIdescPV = idesc_e4m3(kTileM, C::OTW, true);
+            int pv_uses = 0;
+            bool ok = W.wait(BAR(C::B_Q), 0);
+            ptx::tc_fence_after();
+            auto do_pv = [&](int j) -> bool {
+                const int sb = j % C::NS;
+                const int vs = j % C::STAGES;
+                if (!W.wait(BAR(C::B_PF + sb), (uint32_t)(j / C::NS) & 1u)) return false;
+                if (!W.wait(BAR(C::B_VF + vs), (uint32_t)(j / C::STAGES) & 1u)) return false;
+                ptx::tc_fence_after();
+                const uint32_t vbase = sV + vs * C::V_BYTES;
+#pragma unroll
+                for (int c = 0; c < C::NPV; ++c) {
+                    if (!W.wait(BAR(C::B_OE), ((uint32_t)pv_uses & 1u) ^ 1u)) return false;
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kTileN / 32; ++kk) {
+                        const uint32_t a = tmem + C::TM_S + sb * 128 + kk * 8;
+                        const uint64_t bd =
+                            sdesc(vbase + (c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV,
+                                  C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
+                        ptx::mma_f8_ts(tmem + C::TM_OT, a, bd, kIdescPV, kk > 0 ? 1u : 0u);
+                    }
+                    ptx::tc_commit(BAR(C::B_OF));
+                    ++pv_uses;
+                }
+                ptx::tc_commit(BAR(C::B_VE + vs));
+                return true;
+            };
+            for (int it = 0; ok && it < n_tiles; ++it) {
+                const int ks = it % C::STAGES;
+                if (!W.wait(BAR(C::B_KF + ks), (uint32_t)(it / C::STAGES) & 1u)) { ok = false; break; }
+                ptx::tc_fence_after();
+                if (C::NS == 1 && it > 0 && !do_pv(it - 1)) { ok = false; break; }
+                const int sb = it % C::NS;
+                const uint32_t kbase = sK + ks * C::K_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 32; ++kk) {
+                    const int chunk = (kk * 32) / C::CW;
+                    const int off = (kk * 32) % C::CW;
+                    const uint64_t qd = sdesc(sQ + chunk * C::CHUNK_Q + off, 16, 8 * C::CW, swz_layout(C::CW));
+                    const uint64_t kd = sdesc(kbase + chunk * C::CHUNK_K + off, 16, 8 * C::CW, swz_layout(C::CW));
+                    ptx::mma_f8_ss(tmem + C::TM_S + sb * 128, qd, kd, kIdescQK, kk > 0 ? 1u : 0u);
+                }
+                ptx::tc_commit(BAR(C::B_SF + sb));
+                ptx::tc_commit(BAR(C::B_KE + ks));
+                if (C::NS == 2 && it > 0 && !do_pv(it - 1)) { ok = false; break; }
+            }
+            if (ok) ok = do_pv(n_tiles - 1);
+            // all MMAs must finish before TMEM is released
+            ptx::tc_commit(BAR(C::B_DONE));
+            W.drain(BAR(C::B_DONE), 0);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ======================================================== softmax
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const bool warp_active = __any_sync(0xffffffffu, row_ok);
+        const float dqv = p.dq ? p.dq[b * p.dq_sb + kvh * p.dq_sh] : 1.f;
+        const float dkv = p.dk ? p.dk[b * p.dk_sb + kvh * p.dk_sh] : 1.f;
+        const float dvv = p.dv ? p.dv[b * p.dv_sb + kvh * p.dv_sh] : 1.f;
+        const float c = p.scale_log2 * dqv * dkv;
+        const int hi_row = p.causal ? min(Lk - 1, rpos + delta) : Lk - 1;
+        const int lo_row = p.window_left >= 0 ? max(0, rpos + delta - p.window_left) : 0;
+        float m_run = -INFINITY, row_sum = 0.f;
+        for (int it = 0; it < n_tiles; ++it) {
+            const int k0 = (t_beg + it) * kTileN;
+            const int sb = it % C::NS;
+            if (!W.wait(BAR(C::B_SF + sb), (uint32_t)(it / C::NS) & 1u)) break;
+            ptx::tc_fence_after();
+            float alpha = 1.f;
+            if (warp_active) {
+                uint32_t u[4][32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ptx::tmem_ld32(tmem + lane_base + C::TM_S + sb * 128 + 32 * j, u[j]);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ptx::reg_fence32(u[j]);
+                float s[128];
+#pragma unroll
+                for (int i = 0; i < 128; ++i) s[i] = u2f(u[i >> 5][i & 31]);
+                const bool need_mask = (k0 + kTileN > Lk) || (p.causal && k0 + kTileN - 1 > pos0 + delta) ||
+                                       (p.window_left >= 0 && k0 < pos_last + delta - p.window_left);
+                if (need_mask) {
+                    const int hi = hi_row - k0, lo = lo_row - k0;
+#pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        if (i > hi || i < lo) s[i] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+                const float mt = mx * c;
+                if (mt > m_run + kTau) {
+                    alpha = ptx::ex2(m_run - mt);
+                    row_sum *= alpha;
+                    m_run = mt;
+                }
+                const float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
+                float sum = 0.f;
+                uint32_t w[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float p0 = ptx::ex2(fmaf(s[4 * k + 0], c, bias));
+                    const float p1 = ptx::ex2(fmaf(s[4 * k + 1], c, bias));
+                    const float p2 = ptx::ex2(fmaf(s[4 * k + 2], c, bias));
+                    const float p3 = ptx::ex2(fmaf(s[4 * k + 3], c, bias));
+                    sum += (p0 + p1) + (p2 + p3);
+                    w[k] = ptx::cvt_e4m3x2(p1, p0) | (ptx::cvt_e4m3x2(p3, p2) << 16);
+                }
+                ptx::tmem_st32(tmem + lane_base + C::TM_S + sb * 128, w);
+                ptx::tmem_wait_st();
+                row_sum += sum;
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(BAR(C::B_PF + sb));
+            if (!W.wait(BAR(C::B_AE + (it & 1)), ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
+            alpha_ring[(it & 1) * 128 + r] = alpha;
+            ptx::mbar_arrive(BAR(C::B_AF + (it & 1)));
+        }
+        // finalize: the 2^8 bias cancels between O and row_sum and is removed from the LSE
+        float scale_o = 0.f, lse;
+        const float sig = has_sink ? p.sink[hq] : 0.f;
+        if (m_run == -INFINITY) {
+            lse = has_sink ? sig : -INFINITY;
+        } else {
+            const float sl2 = sig * kLog2e;
+            const float m_f = (has_sink && sl2 > m_run) ? sl2 : m_run;
+            const float sc = ptx::ex2(m_run - m_f);
+            const float rs = row_sum * sc + (has_sink ? ptx::ex2(sl2 - m_f + kPBias) : 0.f);
+            scale_o = sc * dvv / rs;
+            lse = (ptx::lg2(rs) + m_f - kPBias) * kLn2;
+        }
+        row_scale[r] = scale_o;
+        if (row_ok) {
+            if (p.split_mode)
+                p.lse_part[((long long)split * p.total_q + tok) * p.Hq + hq] = lse;
+            else if (p.lse)
+                p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
+        }
+        ptx::named_bar_sync(1, 256);
+    } else {
+        // ======================================================== correction (warps 4-7)
+        const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+        const bool warp_active = __any_sync(0xffffffffu, row_ok);
+        float o[C::O_REGS ? DV : 1];
+#pragma unroll
+        for (int i = 0; i < (C::O_REGS ? DV : 1); ++i) o[i] = 0.f;
+        int pv_uses = 0;
+        bool ok = true;
+        for (int it = 0; ok && it < n_tiles; ++it) {
+            if (!W.wait(BAR(C::B_AF + (it & 1)), (uint32_t)(it >> 1) & 1u)) break;
+            const float alpha = alpha_ring[(it & 1) * 128 + r];
+            ptx::mbar_arrive(BAR(C::B_AE + (it & 1)));
+#pragma unroll
+            for (int c = 0; c < C::NPV; ++c) {
+                if (!W.wait(BAR(C::B_OF), (uint32_t)pv_uses & 1u)) { ok = false; break; }
+                ptx::tc_fence_after();
+                if (warp_active) {
+#pragma unroll
+                    for (int j = 0; j < C::OTW / 32; ++j) {
+                        uint32_t u[32];
+                        ptx::tmem_ld32(tmem + lane_base + C::TM_OT + 32 * j, u);
+                        if constexpr (C::O_REGS) {
+                            ptx::tmem_wait_ld();
+                            ptx::reg_fence32(u);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int idx = (C::O_REGS ? (c * C::OTW + 32 * j + i) : 0);
+                                o[idx] = (it == 0) ? u2f(u[i]) : fmaf(o[idx], alpha, u2f(u[i]));
+                            }
+                        } else {
+                            const uint32_t orun = tmem + lane_base + C::TM_OR + c * C::OTW + 32 * j;
+                            uint32_t v[32];
+                            if (it > 0) {
+                                ptx::tmem_ld32(orun, v);
+                                ptx::tmem_wait_ld();
+                                ptx::reg_fence32(u);
+                                ptx::reg_fence32(v);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(fmaf(u2f(v[i]), alpha, u2f(u[i])));
+                            } else {
+                                ptx::tmem_wait_ld();
+                                ptx::reg_fence32(u);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = u[i];
+                            }
+                            ptx::tmem_st32(orun, v);
+                            ptx::tmem_wait_st();
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(BAR(C::B_OE));
+                ++pv_uses;
+            }
+        }
+        ptx::named_bar_sync(1, 256);
+        const float sc = row_scale[r];
+        if (row_ok) {
+            if (p.split_mode) {
+                float *dst = p.o_part + (((long long)split * p.total_q + tok) * p.Hq + hq) * DV;
+                if constexpr (C::O_REGS) {
+#pragma unroll
+                    for (int i = 0; i < DV; i += 4)
+                        *reinterpret_cast<float4 *>(dst + i) =
+                            make_float4(o[i] * sc, o[i + 1] * sc, o[i + 2] * sc, o[i + 3] * sc);
+                } else {
+#pragma unroll 1
+                    for (int j = 0; j < DV / 32; ++j) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(tmem + lane_base + C::TM_OR + 32 * j, v);
+                        ptx::tmem_wait_ld();
+                        ptx::reg_fence32(v);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4 *>(dst + 32 * j + i) = make_float4(
+                                u2f(v[i]) * sc, u2f(v[i + 1]) * sc, u2f(v[i + 2]) * sc, u2f(v[i + 3]) * sc);
+                    }
+                }
+            } else {
+                uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + 2 * (beta * p.o_sb + rho * p.o_ss + hq * p.o_sh);
+                if constexpr (C::O_REGS) {
+#pragma unroll
+                    for (int i = 0; i < DV; i += 8) {
+                        float t8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) t8[e] = o[i + e] * sc;
+                        store8(dst + 2 * i, t8, p.out_fp16);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int j = 0; j < DV / 32; ++j) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(tmem + lane_base + C::TM_OR + 32 * j, v);
+                        ptx::tmem_wait_ld();
+                        ptx::reg_fence32(v);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8) {
+                            float t8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) t8[e] = u2f(v[i + e]) * sc;
+                            store8(dst + 2 * (32 * j + i), t8, p.out_fp16);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    // ------------------------------------------------------------ teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+// Split-KV merge: one warp per (token, q-head) row.
+//   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
+// Splits with LSE_s = -inf contribute nothing (their O_s is zero).
+template <int DV>
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
+    constexpr int PER = DV / 32;  // output columns per lane
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * 8 + warp;
+    if (row >= (long long)p.total_q * p.Hq) return;
+    const int tok = (int)(row / p.Hq);
+    const int hq = (int)(row % p.Hq);
+    const long long stride_s = (long long)p.total_q * p.Hq;
+    float m = -INFINITY;
+    for (int s = lane; s < p.num_splits; s += 32) m = fmaxf(m, p.lse_part[s * stride_s + row]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    float lse = -INFINITY;
+    if (m != -INFINITY) {
+        float sw = 0.f;
+        for (int s = lane; s < p.num_splits; s += 32) {
+            const float l = p.lse_part[s * stride_s + row];
+            if (l != -INFINITY) sw += ptx::ex2((l - m) * kLog2e);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
+        lse = m + ptx::lg2(sw) * kLn2;
+        const float inv = 1.f / sw;
+        bool first = true;
+        for (int s = 0; s < p.num_splits; ++s) {
+            const float l = p.lse_part[s * stride_s + row];
+            if (l == -INFINITY) continue;
+            const float wgt = ptx::ex2((l - m) * kLog2e) * inv;
+            const float *src = p.o_part + (s * stride_s + row) * DV + lane * PER;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) acc[i] = first ? wgt * src[i] : fmaf(wgt, src[i], acc[i]);
+            first = false;
+        }
+    }
+    const long long beta = p.q_varlen ? 0 : tok / p.Sq;
+    const long long rho = p.q_varlen ? tok : tok % p.Sq;
+    if (lane == 0 && p.lse) p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
+    uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + 2 * (beta * p.o_sb + rho * p.o_ss + hq * p.o_sh + lane * PER);
+#pragma unroll
+    for (int i = 0; i < PER; i += 2) {
+        uint32_t w;
+        if (p.out_fp16) {
+            __half2 h = __floats2half2_rn(acc[i], acc[i + 1]);
+            w = *reinterpret_cast<uint32_t *>(&h);
+        } else {
+            __nv_bfloat162 h = __floats2bfloat162_rn(acc[i], acc[i + 1]);
+            w = *reinterpret_cast<uint32_t *>(&h);
+        }
+        *reinterpret_cast<uint32_t *>(dst + 2 * i) = w;
+    }
+}
+
+// One CTA, one thread: a bounded wait on a barrier that nothing completes.
+__global__ void wait_probe_kernel(unsigned long long timeout_ns, unsigned int *status);
+
+}  // namespace fa8

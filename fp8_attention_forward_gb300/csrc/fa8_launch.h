@@ -1,0 +1,36 @@
+// fa8_launch.h -- internal: typed launchers, one translation unit per head-dim pair so the
+// instantiations compile in parallel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa8_kernel.cuh"
+
+namespace fa8 {
+
+template <int D, int DV>
+cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, dim3 grid, cudaStream_t stream);
+
+template <int DV>
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+
+// Defines launch_fwd<D, DV>.  Dynamic shared memory above 48 KB needs an opt-in per
+// function and device; it is set on every launch (a cheap host call) so that a first
+// launch on a new device needs no extra bookkeeping.
+#define FA8_DEFINE_FWD(D_, DV_)                                                              \
+    template <>                                                                              \
+    cudaError_t launch_fwd<D_, DV_>(const FwdParams &p, const CUtensorMap &tq,               \
+                                    const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid, \
+                                    cudaStream_t stream) {                                   \
+        constexpr int smem = Cfg<D_, DV_>::SMEM_BYTES;                                       \
+        cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D_, DV_>,                            \
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,    \
+                                             smem);                                          \
+        if (e != cudaSuccess) return e;                                                      \
+        fwd_kernel<D_, DV_><<<grid, kNumThreads, smem, stream>>>(p, tq, tk, tv);             \
+        return cudaGetLastError();                                                           \
+    }
+
+}  // namespace fa8
