@@ -176,6 +176,12 @@ struct Waiter {
             }
         }
     }
+    // Whole-warp form: every lane waits, the result is made warp-uniform and the warp is
+    // reconverged (needed before the warp-collective tcgen05.ld/st that follow).
+    __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) const {
+        const bool ok = wait(bar, parity);
+        return __all_sync(0xffffffffu, ok);
+    }
     // Used when draining in-flight async work before exit: ignores the abort flag.
     __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
         const uint64_t t0 = ptx::globaltimer();
@@ -414,7 +420,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int c2 = p.kv_mode == 1 ? k_start + k0 : k0;
             const int c3 = p.kv_mode == 1 ? 0 : b;
             // K tile
-            if (!W.wait(BAR(C::B_KE + st), ph ^ 1u)) break;
+            if (!W.wait_warp(BAR(C::B_KE + st), ph ^ 1u)) break;
             if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_KF + st), (uint32_t)C::K_BYTES);
             __syncwarp();
             const uint32_t dK = sK + st * C::K_BYTES;
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             issued_k = it + 1;
             // V tile
-            if (!W.wait(BAR(C::B_VE + st), ph ^ 1u)) break;
+            if (!W.wait_warp(BAR(C::B_VE + st), ph ^ 1u)) break;
             if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_VF + st), (uint32_t)C::V_BYTES);
             __syncwarp();
             const uint32_t dV = sV + st * C::V_BYTES;
@@ -532,7 +538,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int it = 0; it < n_tiles; ++it) {
             const int k0 = (t_beg + it) * kTileN;
             const int sb = it % C::NS;
-            if (!W.wait(BAR(C::B_SF + sb), (uint32_t)(it / C::NS) & 1u)) break;
+            if (!W.wait_warp(BAR(C::B_SF + sb), (uint32_t)(it / C::NS) & 1u)) break;
             ptx::tc_fence_after();
             float alpha = 1.f;
             if (warp_active) {
@@ -580,7 +586,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(BAR(C::B_PF + sb));
-            if (!W.wait(BAR(C::B_AE + (it & 1)), ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
+            if (!W.wait_warp(BAR(C::B_AE + (it & 1)), ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
             alpha_ring[(it & 1) * 128 + r] = alpha;
             ptx::mbar_arrive(BAR(C::B_AF + (it & 1)));
         }
@@ -615,12 +621,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         int pv_uses = 0;
         bool ok = true;
         for (int it = 0; ok && it < n_tiles; ++it) {
-            if (!W.wait(BAR(C::B_AF + (it & 1)), (uint32_t)(it >> 1) & 1u)) break;
+            if (!W.wait_warp(BAR(C::B_AF + (it & 1)), (uint32_t)(it >> 1) & 1u)) break;
             const float alpha = alpha_ring[(it & 1) * 128 + r];
             ptx::mbar_arrive(BAR(C::B_AE + (it & 1)));
 #pragma unroll
             for (int c = 0; c < C::NPV; ++c) {
-                if (!W.wait(BAR(C::B_OF), (uint32_t)pv_uses & 1u)) { ok = false; break; }
+                if (!W.wait_warp(BAR(C::B_OF), (uint32_t)pv_uses & 1u)) { ok = false; break; }
                 ptx::tc_fence_after();
                 if (warp_active) {
 #pragma unroll
@@ -663,14 +669,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         ptx::named_bar_sync(1, 256);
         const float sc = row_scale[r];
-        if (row_ok) {
+        // TMEM loads are warp-collective (.sync.aligned): the whole active warp loads, only
+        // the valid rows store.
+        if (warp_active) {
             if (p.split_mode) {
                 float *dst = p.o_part + (((long long)split * p.total_q + tok) * p.Hq + hq) * DV;
                 if constexpr (C::O_REGS) {
+                    if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < DV; i += 4)
-                        *reinterpret_cast<float4 *>(dst + i) =
-                            make_float4(o[i] * sc, o[i + 1] * sc, o[i + 2] * sc, o[i + 3] * sc);
+                        for (int i = 0; i < DV; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) =
+                                make_float4(o[i] * sc, o[i + 1] * sc, o[i + 2] * sc, o[i + 3] * sc);
+                    }
                 } else {
 #pragma unroll 1
                     for (int j = 0; j < DV / 32; ++j) {
@@ -678,21 +688,25 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         ptx::tmem_ld32(tmem + lane_base + C::TM_OR + 32 * j, v);
                         ptx::tmem_wait_ld();
                         ptx::reg_fence32(v);
+                        if (row_ok) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(dst + 32 * j + i) = make_float4(
-                                u2f(v[i]) * sc, u2f(v[i + 1]) * sc, u2f(v[i + 2]) * sc, u2f(v[i + 3]) * sc);
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4 *>(dst + 32 * j + i) = make_float4(
+                                    u2f(v[i]) * sc, u2f(v[i + 1]) * sc, u2f(v[i + 2]) * sc, u2f(v[i + 3]) * sc);
+                        }
                     }
                 }
             } else {
                 uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + 2 * (beta * p.o_sb + rho * p.o_ss + hq * p.o_sh);
                 if constexpr (C::O_REGS) {
+                    if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < DV; i += 8) {
-                        float t8[8];
+                        for (int i = 0; i < DV; i += 8) {
+                            float t8[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) t8[e] = o[i + e] * sc;
-                        store8(dst + 2 * i, t8, p.out_fp16);
+                            for (int e = 0; e < 8; ++e) t8[e] = o[i + e] * sc;
+                            store8(dst + 2 * i, t8, p.out_fp16);
+                        }
                     }
                 } else {
 #pragma unroll 1
@@ -701,12 +715,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         ptx::tmem_ld32(tmem + lane_base + C::TM_OR + 32 * j, v);
                         ptx::tmem_wait_ld();
                         ptx::reg_fence32(v);
+                        if (row_ok) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 8) {
-                            float t8[8];
+                            for (int i = 0; i < 32; i += 8) {
+                                float t8[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) t8[e] = u2f(v[i + e]) * sc;
-                            store8(dst + 2 * (32 * j + i), t8, p.out_fp16);
+                                for (int e = 0; e < 8; ++e) t8[e] = u2f(v[i + e]) * sc;
+                                store8(dst + 2 * (32 * j + i), t8, p.out_fp16);
+                            }
                         }
                     }
                 }
