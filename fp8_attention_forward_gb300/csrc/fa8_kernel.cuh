@@ -17,6 +17,9 @@
 //   P_t   = 2^(s*c - m + 8) -> E4M3 (c = softmax_scale * dq * dk * log2 e), stored
 //         in TMEM over the first 32 columns of S_t
 //   O_t   = P_t V_t                     accumulated from zero for every tile
+//         (on tiles that need a mask, P_t = P_hi + P_lo with P_lo = e4m3(p - P_hi) and
+//          both terms go through the PV MMA: rows with only a few visible keys keep
+//          ~2^-8 relative precision instead of the 2^-4 of one E4M3 term)
 //   O     = O * alpha + O_t             fp32 fold (two-level accumulation)
 // and after the last tile O * dv / rowsum -> bf16/fp16, LSE = ln2*(log2 rowsum + m - 8).
 #pragma once
@@ -194,6 +197,14 @@ struct Waiter {
         return true;
     }
 };
+
+// Whether any row of the tile (keys [k0, k0+128)) needs masking: CTA-uniform; the
+// softmax and MMA roles both evaluate it so that they agree on the two-term P.
+__device__ __forceinline__ bool tile_needs_mask(int k0, int Lk, int causal, int window_left, int pos0,
+                                                int pos_last, int delta) {
+    return (k0 + kTileN > Lk) || (causal && k0 + kTileN - 1 > pos0 + delta) ||
+           (window_left >= 0 && k0 < pos_last + delta - window_left);
+}
 
 // Maps a varlen grid slot to (request, m-block): the slots enumerate each request's
 // m-blocks in order; within a request the m-block order is reversed so that, with a
@@ -481,6 +492,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 if (!W.wait(BAR(C::B_VF + vs), (uint32_t)(j / C::STAGES) & 1u)) return false;
                 ptx::tc_fence_after();
                 const uint32_t vbase = sV + vs * C::V_BYTES;
+                const bool two_term = tile_needs_mask((t_beg + j) * kTileN, Lk, p.causal, p.window_left, pos0,
+                                                      pos_last, delta);
 #pragma unroll
                 for (int c = 0; c < C::NPV; ++c) {
                     if (!W.wait(BAR(C::B_OE), ((uint32_t)pv_uses & 1u) ^ 1u)) return false;
@@ -492,6 +505,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             sdesc(vbase + (c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV,
                                   C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
                         ptx::mma_f8_ts(tmem + C::TM_OT, a, bd, kIdescPV, kk > 0 ? 1u : 0u);
+                    }
+                    if (two_term) {  // + P_lo V (P_lo in the next 32 columns)
+#pragma unroll
+                        for (int kk = 0; kk < kTileN / 32; ++kk) {
+                            const uint32_t a = tmem + C::TM_S + sb * 128 + 32 + kk * 8;
+                            const uint64_t bd =
+                                sdesc(vbase + (c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV,
+                                      C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
+                            ptx::mma_f8_ts(tmem + C::TM_OT, a, bd, kIdescPV, 1u);
+                        }
                     }
                     ptx::tc_commit(BAR(C::B_OF));
                     ++pv_uses;
@@ -551,8 +574,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 float s[128];
 #pragma unroll
                 for (int i = 0; i < 128; ++i) s[i] = u2f(u[i >> 5][i & 31]);
-                const bool need_mask = (k0 + kTileN > Lk) || (p.causal && k0 + kTileN - 1 > pos0 + delta) ||
-                                       (p.window_left >= 0 && k0 < pos_last + delta - p.window_left);
+                const bool need_mask = tile_needs_mask(k0, Lk, p.causal, p.window_left, pos0, pos_last, delta);
                 if (need_mask) {
                     const int hi = hi_row - k0, lo = lo_row - k0;
 #pragma unroll
@@ -571,16 +593,37 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
                 float sum = 0.f;
                 uint32_t w[32];
+                if (!need_mask) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float p0 = ptx::ex2(fmaf(s[4 * k + 0], c, bias));
-                    const float p1 = ptx::ex2(fmaf(s[4 * k + 1], c, bias));
-                    const float p2 = ptx::ex2(fmaf(s[4 * k + 2], c, bias));
-                    const float p3 = ptx::ex2(fmaf(s[4 * k + 3], c, bias));
-                    sum += (p0 + p1) + (p2 + p3);
-                    w[k] = ptx::cvt_e4m3x2(p1, p0) | (ptx::cvt_e4m3x2(p3, p2) << 16);
+                    for (int k = 0; k < 32; ++k) {
+                        const float p0 = ptx::ex2(fmaf(s[4 * k + 0], c, bias));
+                        const float p1 = ptx::ex2(fmaf(s[4 * k + 1], c, bias));
+                        const float p2 = ptx::ex2(fmaf(s[4 * k + 2], c, bias));
+                        const float p3 = ptx::ex2(fmaf(s[4 * k + 3], c, bias));
+                        sum += (p0 + p1) + (p2 + p3);
+                        w[k] = ptx::cvt_e4m3x2(p1, p0) | (ptx::cvt_e4m3x2(p3, p2) << 16);
+                    }
+                    ptx::tmem_st32(tmem + lane_base + C::TM_S + sb * 128, w);
+                } else {
+                    // two E4M3 terms: P_hi = e4m3(p) in columns [0,32), P_lo = e4m3(p - P_hi) in [32,64)
+                    uint32_t wl[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        float pv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) pv[e] = ptx::ex2(fmaf(s[4 * k + e], c, bias));
+                        sum += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+                        const uint32_t h01 = ptx::cvt_e4m3x2(pv[1], pv[0]);
+                        const uint32_t h23 = ptx::cvt_e4m3x2(pv[3], pv[2]);
+                        float q0, q1, q2, q3;
+                        ptx::e4m3x2_to_f32(h01, q0, q1);
+                        ptx::e4m3x2_to_f32(h23, q2, q3);
+                        w[k] = h01 | (h23 << 16);
+                        wl[k] = ptx::cvt_e4m3x2(pv[1] - q1, pv[0] - q0) | (ptx::cvt_e4m3x2(pv[3] - q3, pv[2] - q2) << 16);
+                    }
+                    ptx::tmem_st32(tmem + lane_base + C::TM_S + sb * 128, w);
+                    ptx::tmem_st32(tmem + lane_base + C::TM_S + sb * 128 + 32, wl);
                 }
-                ptx::tmem_st32(tmem + lane_base + C::TM_S + sb * 128, w);
                 ptx::tmem_wait_st();
                 row_sum += sum;
             }

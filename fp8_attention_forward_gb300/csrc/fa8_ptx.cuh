@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace fa8 {
@@ -170,6 +171,15 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return static_cast<uint32_t>(r);
+}
+
+// Unpacks two E4M3 bytes (bits 0..7 -> lo, 8..15 -> hi) to fp32, exactly.
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t pair, float &lo, float &hi) {
+    uint32_t h2;
+    const uint16_t b = static_cast<uint16_t>(pair);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(b));
+    lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+    hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
 }
 
 }  // namespace ptx

@@ -36,14 +36,16 @@ def v_scale(case):
     for b, lk in enumerate(case.seqlens_k):
         if lk == 0:
             continue
+        v8 = case.v.view(torch.uint8)  # byte view: float8 tensors cannot be indexed everywhere
         if case.kv_layout == "batched":
-            rows = case.v[b]
+            rows = v8[b]
         elif case.kv_layout == "varlen":
-            rows = case.v[off:off + lk]
+            rows = v8[off:off + lk]
         else:
             pages = case.block_table[b, : (lk + case.page_size - 1) // case.page_size].long()
-            rows = case.v[pages.to(case.v.device)].reshape(-1, case.Hkv, case.DV)[:lk]
+            rows = v8[pages.to(case.v.device)].reshape(-1, case.Hkv, case.DV)[:lk]
         off += lk
+        rows = rows.view(torch.float8_e4m3fn)
         ms = rows.float().pow(2).mean(dim=(0, 2)).double().cpu().numpy()
         out[b] = np.sqrt(ms) * dv[b]
     return out
