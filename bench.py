@@ -1,0 +1,341 @@
+"""Benchmark of the fused FP8 attention forward on one GB300 (or N replicas).
+
+Headline: causal GQA prefill (B=2, Hq=32, Hkv=8, S=4096, d=dv=128, E4M3 in, bf16 out) in
+TFLOP/s of algorithmic work (2*(d+dv) flops per unmasked (row, key) pair), against the
+dense FP8 tensor peak.  The same line carries the paged decode workload (B=64, 1 token,
+Hq=64, Hkv=8, d=dv=128, 16-token pages, keys ~U[1024,32768]) in GB/s against HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Timing: W untimed steps, then K steps; before every step a 256 MB buffer is written to
+flush L2 (129 MB); each step's forward call is bracketed by CUDA events on the launching
+stream; ms_per_step is the mean over the K steps, max over ranks.  `e2e` repeats the
+measurement through the public call with the inputs copied from pinned host memory and
+the output copied back inside the timed region.  `--impl reference` times the fp64 CPU
+oracle (the only reference this path has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp8_attention_forward_gb300 import inputs  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+METRIC = "FP8 attn fwd TFLOP/s (prefill) & decode HBM GB/s; % of GB300 roofline"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="fa8_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_kernel(run, steps, warmup, flush):
+    """Mean device time (ms) of `run()` over `steps` calls, L2 flushed before each."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.fill_(1)
+        run()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush.fill_(1)
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def bench_case(case, steps, warmup, flush, fa8, num_splits=0):
+    """Kernel-only and end-to-end timings of one case (tensors on the GPU)."""
+    splits, ws_bytes, _ = fa8.plan(case.q, case.k, case.v, cu_seqlens_q=case.cu_seqlens_q,
+                                   cu_seqlens_k=case.cu_seqlens_k, block_table=case.block_table,
+                                   page_size=case.page_size, num_splits=num_splits)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty(tuple(case.q.shape[:-1]) + (case.DV,), dtype=case.out_dtype, device="cuda")
+    lse = (torch.empty((case.q.shape[0], case.Hq, case.q.shape[1]), dtype=torch.float32, device="cuda")
+           if case.q.dim() == 4 else torch.empty((case.Hq, case.q.shape[0]), dtype=torch.float32, device="cuda"))
+
+    def run():
+        fa8.fwd_case(case, out=out, lse=lse, workspace=ws, num_splits=num_splits)
+
+    times = time_kernel(run, steps, warmup, flush)
+    st = fa8.check()
+    if st != fa8.FA8_SUCCESS:
+        raise RuntimeError(f"device status {st}")
+    launches = 1 + (1 if splits > 1 else 0)
+    return {"ms": statistics.mean(times), "ms_min": min(times), "splits": splits,
+            "launches_per_step": launches, "out": out, "lse": lse, "ws": ws}
+
+
+def bench_e2e(case, steps, warmup, flush, fa8, num_splits=0):
+    """Per step: pinned host -> device copies of Q/K/V (and the small index tensors), the
+    forward, and the output/LSE copied back to pinned host memory."""
+    dev = case
+    host = {}
+    names = ["q", "k", "v", "descale_q", "descale_k", "descale_v", "cu_seqlens_q", "cu_seqlens_k",
+             "block_table", "sink"]
+    for n in names:
+        t = getattr(dev, n)
+        if t is not None:
+            host[n] = t.cpu().pin_memory()
+    dst = {n: torch.empty_like(getattr(dev, n)) for n in host}
+    import dataclasses
+
+    dcase = dataclasses.replace(dev, **dst)
+    splits, ws_bytes, _ = fa8.plan(dcase.q, dcase.k, dcase.v, cu_seqlens_q=dcase.cu_seqlens_q,
+                                   cu_seqlens_k=dcase.cu_seqlens_k, block_table=dcase.block_table,
+                                   page_size=dcase.page_size, num_splits=num_splits)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty(tuple(dcase.q.shape[:-1]) + (dcase.DV,), dtype=dcase.out_dtype, device="cuda")
+    lse = (torch.empty((dcase.q.shape[0], dcase.Hq, dcase.q.shape[1]), dtype=torch.float32, device="cuda")
+           if dcase.q.dim() == 4 else torch.empty((dcase.Hq, dcase.q.shape[0]), dtype=torch.float32, device="cuda"))
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+
+    def run():
+        for n, t in host.items():
+            dst[n].copy_(t, non_blocking=True)
+        fa8.fwd_case(dcase, out=out, lse=lse, workspace=ws, num_splits=num_splits)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    times = time_kernel(run, steps, warmup, flush)
+    return {"ms": statistics.mean(times), "h2d": h2d, "d2h": d2h}
+
+
+def cpu_oracle_sample(case, budget_s=15.0, seed=0):
+    """Times the fp64 oracle (single thread) on randomly sampled output rows of `case`
+    until ~budget_s of CPU work; returns (flop/s, rows, seconds)."""
+    import numpy as np
+
+    import oracle
+
+    arrays = oracle.problem_arrays(case)
+    rng = np.random.default_rng(seed)
+    total_flops = 0.0
+    rows_done = 0
+    t0 = time.perf_counter()
+    lens_q = case.seqlens_q
+    lens_k = case.seqlens_k
+    starts = np.concatenate([[0], np.cumsum(lens_q)])
+    while time.perf_counter() - t0 < budget_s:
+        rows = []
+        for _ in range(8):
+            tok = int(rng.integers(0, case.total_q))
+            rows.append((tok, int(rng.integers(0, case.Hq))))
+        oracle.attention_arrays(arrays, rows=rows)
+        for tok, _ in rows:
+            b = int(np.searchsorted(starts, tok, side="right") - 1)
+            i = tok - starts[b]
+            lq, lk = lens_q[b], lens_k[b]
+            hi = lk - 1
+            if case.causal:
+                hi = min(hi, i + lk - lq)
+            lo = 0 if case.window_left < 0 else max(0, i + lk - lq - case.window_left)
+            total_flops += 2.0 * (case.D + case.DV) * max(0, hi - lo + 1)
+        rows_done += len(rows)
+    dt = time.perf_counter() - t0
+    return total_flops / dt, rows_done, dt
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="fa8", choices=["fa8", "reference"])
+    ap.add_argument("--no-decode", action="store_true", help="skip the paged-decode figure")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    peaks = _peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # dense FP8 = 2x dense bf16 (nominal 4.5 vs 2.25 PF)
+    workload = "causal_gqa_prefill B=2 Hq=32 Hkv=8 Sq=Sk=4096 d=dv=128 e4m3->bf16"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        case = inputs.causal_gqa_prefill("full", device="cpu")
+        flops, rows, dt = cpu_oracle_sample(case, budget_s=args.cpu_budget)
+        val = flops / 1e12
+        sample = f"{rows} random (token, head) rows of the workload, {dt:.1f} s single-thread fp64"
+        line = {"metric": METRIC, "value": val, "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic", "impl": "reference",
+                "config": {"workload": workload, "impl": "fp64 CPU oracle (oracle/attn_ref.c)"},
+                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from fp8_attention_forward_gb300 import build as _build
+    from fp8_attention_forward_gb300 import fa8
+
+    if rank == 0:
+        _build.build()
+    _barrier(world)
+    fa8.lib()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    prefill = inputs.causal_gqa_prefill("full", device="cuda")
+    flops = inputs.algorithmic_flops(prefill)
+
+    _barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    with ClockSampler(local) as clocks:
+        res = bench_case(prefill, args.steps, args.warmup, flush, fa8)
+        torch.cuda.synchronize()
+    _barrier(world)
+    wall = time.perf_counter() - t_wall
+    clk = clocks.summary()
+    ms = _max_over_ranks(res["ms"], world)
+    tflops_rank = flops / (ms * 1e-3) / 1e12
+    value = tflops_rank * world
+
+    e2e = bench_e2e(prefill, max(3, args.steps // 2), 3, flush, fa8)
+    e2e_ms = _max_over_ranks(e2e["ms"], world)
+
+    decode = None
+    if not args.no_decode:
+        dec = inputs.paged_decode("full", device="cuda")
+        dbytes = inputs.algorithmic_bytes(dec)
+        dres = bench_case(dec, args.steps, args.warmup, flush, fa8)
+        dms = _max_over_ranks(dres["ms"], world)
+        gbs = dbytes / (dms * 1e-3) / 1e9
+        decode = {"workload": "paged_decode B=64 Sq=1 Hq=64 Hkv=8 d=dv=128 page=16 keys~U[1024,32768]",
+                  "value": gbs * world, "unit": "GB/s", "ms_per_step": dms, "splits": dres["splits"],
+                  "algorithmic_bytes": dbytes,
+                  "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                               "peak_source": peaks["source"] + " copy bandwidth"}}
+        del dec, dres
+
+    cpu = None
+    if rank == 0:
+        cpu_case = prefill.to("cpu")
+        cflops, crows, cdt = cpu_oracle_sample(cpu_case, budget_s=args.cpu_budget)
+        cpu = {"value": cflops / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{crows} random (token, head) rows of the prefill workload, {cdt:.1f} s, single-thread fp64"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic",
+            "config": {"workload": workload, "global_batch": 2 * world, "seq_len": 4096,
+                       "parallelism": f"replicas x{world}", "l2": "256 MB buffer written before every step",
+                       "flop_convention": "2*(d+dv) per unmasked (row,key) pair",
+                       "algorithmic_flops": flops, "splits": res["splits"]},
+            "roofline": {"bound": "tensor", "achieved": tflops_rank, "peak": fp8_peak, "unit": "TFLOP/s",
+                         "frac": tflops_rank / fp8_peak, "traffic": None,
+                         "peak_source": f"{peaks['source']} bf16 burst x2 (dense FP8 = 2x bf16)"},
+            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e_ms},
+            "gpu_launches": res["launches_per_step"] * args.steps,
+            "clocks": clk, "decode": decode, "cpu_baseline": cpu, "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
