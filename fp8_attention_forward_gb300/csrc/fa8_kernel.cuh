@@ -3,11 +3,12 @@
 //
 // One CTA computes one 128-row Q tile: the rows are (query position, q-head) pairs of one
 // kv-head group, packed position-major (PackGQA), against the kv-head's keys, for one
-// split of the request's key range.  Roles (320 threads):
-//   warps 0-3  softmax: thread r owns TMEM lane r = tile row r
-//   warps 4-7  correction: two-level PV fold into fp32 O, epilogue
-//   warp 8     TMA producer (Q once, K/V tiles into S-stage rings)
-//   warp 9     MMA issuer (lane 0) and TMEM owner
+// split of the request's key range.  Roles (384 threads, three warpgroups):
+//   warps 0-3   softmax: thread r owns TMEM lane r = tile row r
+//   warps 4-7   correction: two-level PV fold into fp32 O, epilogue
+//   warp 8      TMA producer (Q once, K/V tiles into S-stage rings)
+//   warp 9      MMA issuer (lane 0) and TMEM owner
+//   warps 10-11 idle; the third warpgroup gives its registers to the first two
 //
 // Per 128-key tile t (sources: "[Cute,Fwd,Sm90] Native FP8 (E4M3 Q/K/V) forward for
 // Hopper", Design; "tml-fa4 PR #4", Summary and "Correctness fix over #1"):
@@ -35,7 +36,9 @@ namespace fa8 {
 
 constexpr int kTileM = 128;     // Q rows per CTA = TMEM lanes
 constexpr int kTileN = 128;     // keys per KV tile
-constexpr int kNumThreads = 320;
+constexpr int kNumThreads = 384;
+constexpr int kRegsMath = 224;  // softmax and correction warpgroups after setmaxnreg
+constexpr int kRegsCtl = 48;    // producer / MMA warpgroup (128 x 48 + 256 x 224 <= 384 x 168)
 constexpr float kTau = 0.75f;   // lazy-rescale threshold, log2 units
 constexpr float kPBias = 8.0f;  // P carries a factor 2^8
 constexpr float kLog2e = 1.4426950408889634f;
@@ -96,9 +99,10 @@ struct Cfg {
     static constexpr int NS = O_REGS ? 2 : 1;  // S/P buffers in TMEM
     static constexpr int OTW = (NS * 128 + DV + (O_REGS ? 0 : DV) <= 512) ? DV : DV / 2;
     static constexpr int NPV = DV / OTW;  // PV MMAs per tile (dv split through one O_tile)
+    static constexpr int NOT = O_REGS ? 2 : 1;  // O_tile buffers (double-buffered when O is in registers)
     static constexpr uint32_t TM_S = 0;
     static constexpr uint32_t TM_OT = NS * 128;
-    static constexpr uint32_t TM_OR = TM_OT + OTW;
+    static constexpr uint32_t TM_OR = TM_OT + NOT * OTW;
     static constexpr uint32_t TM_COLS = 512;
     static constexpr int CHUNK_Q = kTileM * CW;
     static constexpr int CHUNK_K = kTileN * CW;
@@ -123,9 +127,9 @@ struct Cfg {
     static constexpr int B_VE = B_VF + STAGES;
     static constexpr int B_SF = B_VE + STAGES;
     static constexpr int B_PF = B_SF + NS;
-    static constexpr int B_OF = B_PF + NS;
-    static constexpr int B_OE = B_OF + 1;
-    static constexpr int B_AF = B_OE + 1;  // 2 slots
+    static constexpr int B_OF = B_PF + NS;   // NOT slots
+    static constexpr int B_OE = B_OF + NOT;  // NOT slots
+    static constexpr int B_AF = B_OE + NOT;  // 2 slots
     static constexpr int B_AE = B_AF + 2;  // 2 slots
     static constexpr int B_DONE = B_AE + 2;
     static constexpr int NUM_BARS = B_DONE + 1;
@@ -373,8 +377,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_init(BAR(C::B_SF + i), 1);
             ptx::mbar_init(BAR(C::B_PF + i), 128);
         }
-        ptx::mbar_init(BAR(C::B_OF), 1);
-        ptx::mbar_init(BAR(C::B_OE), 128);
+        for (int i = 0; i < C::NOT; ++i) {
+            ptx::mbar_init(BAR(C::B_OF + i), 1);
+            ptx::mbar_init(BAR(C::B_OE + i), 128);
+        }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(BAR(C::B_AF + i), 128);
             ptx::mbar_init(BAR(C::B_AE + i), 128);
@@ -399,7 +405,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const Waiter W{abort_flag, p.timeout_ns, p.status};
 
-    if (warp == 8) {
+    if (warp >= 8) {
+      ptx::setmaxnreg_dec<kRegsCtl>();
+      if (warp == 8) {
         // ======================================================== TMA producer
         const bool paged = p.kv_mode == 2;
         int issued_k = 0, issued_v = 0;
@@ -496,7 +504,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                                       pos_last, delta);
 #pragma unroll
                 for (int c = 0; c < C::NPV; ++c) {
-                    if (!W.wait(BAR(C::B_OE), ((uint32_t)pv_uses & 1u) ^ 1u)) return false;
+                    const int ob = pv_uses % C::NOT;
+                    const uint32_t otile = tmem + C::TM_OT + ob * C::OTW;
+                    if (!W.wait(BAR(C::B_OE + ob), ((uint32_t)(pv_uses / C::NOT) & 1u) ^ 1u)) return false;
                     ptx::tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kTileN / 32; ++kk) {
@@ -504,7 +514,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         const uint64_t bd =
                             sdesc(vbase + (c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV,
                                   C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
-                        ptx::mma_f8_ts(tmem + C::TM_OT, a, bd, kIdescPV, kk > 0 ? 1u : 0u);
+                        ptx::mma_f8_ts(otile, a, bd, kIdescPV, kk > 0 ? 1u : 0u);
                     }
                     if (two_term) {  // + P_lo V (P_lo in the next 32 columns)
 #pragma unroll
@@ -513,10 +523,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             const uint64_t bd =
                                 sdesc(vbase + (c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV,
                                       C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
-                            ptx::mma_f8_ts(tmem + C::TM_OT, a, bd, kIdescPV, 1u);
+                            ptx::mma_f8_ts(otile, a, bd, kIdescPV, 1u);
                         }
                     }
-                    ptx::tc_commit(BAR(C::B_OF));
+                    ptx::tc_commit(BAR(C::B_OF + ob));
                     ++pv_uses;
                 }
                 ptx::tc_commit(BAR(C::B_VE + vs));
@@ -547,7 +557,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             W.drain(BAR(C::B_DONE), 0);
         }
         __syncwarp();
-    } else if (warp < 4) {
+      }
+    } else {
+      ptx::setmaxnreg_inc<kRegsMath>();
+      if (warp < 4) {
         // ======================================================== softmax
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const bool warp_active = __any_sync(0xffffffffu, row_ok);
@@ -555,6 +568,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const float dkv = p.dk ? p.dk[b * p.dk_sb + kvh * p.dk_sh] : 1.f;
         const float dvv = p.dv ? p.dv[b * p.dv_sb + kvh * p.dv_sh] : 1.f;
         const float c = p.scale_log2 * dqv * dkv;
+        const uint64_t c2 = ptx::f2pack(c, c);
         const int hi_row = p.causal ? min(Lk - 1, rpos + delta) : Lk - 1;
         const int lo_row = p.window_left >= 0 ? max(0, rpos + delta - p.window_left) : 0;
         float m_run = -INFINITY, row_sum = 0.f;
@@ -581,9 +595,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     for (int i = 0; i < 128; ++i)
                         if (i > hi || i < lo) s[i] = -INFINITY;
                 }
-                float mx = s[0];
+                // row max: eight independent three-input chains of 16, then a small tree
+                float mq[8];
 #pragma unroll
-                for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+                for (int q = 0; q < 8; ++q) {
+                    float m = ptx::fmax3(s[16 * q], s[16 * q + 1], s[16 * q + 2]);
+#pragma unroll
+                    for (int i = 3; i < 15; i += 2) m = ptx::fmax3(m, s[16 * q + i], s[16 * q + i + 1]);
+                    mq[q] = fmaxf(m, s[16 * q + 15]);
+                }
+                const float mx = fmaxf(ptx::fmax3(mq[0], mq[1], mq[2]),
+                                       ptx::fmax3(ptx::fmax3(mq[3], mq[4], mq[5]), mq[6], mq[7]));
                 const float mt = mx * c;
                 if (mt > m_run + kTau) {
                     alpha = ptx::ex2(m_run - mt);
@@ -591,41 +613,57 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     m_run = mt;
                 }
                 const float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
-                float sum = 0.f;
-                uint32_t w[32];
-                if (!need_mask) {
+                const uint64_t b2 = ptx::f2pack(bias, bias);
+                uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
+                const uint32_t pcol = tmem + lane_base + C::TM_S + sb * 128;
+                // P in four chunks of 32 keys (8 TMEM columns of packed E4M3 each)
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float p0 = ptx::ex2(fmaf(s[4 * k + 0], c, bias));
-                        const float p1 = ptx::ex2(fmaf(s[4 * k + 1], c, bias));
-                        const float p2 = ptx::ex2(fmaf(s[4 * k + 2], c, bias));
-                        const float p3 = ptx::ex2(fmaf(s[4 * k + 3], c, bias));
-                        sum += (p0 + p1) + (p2 + p3);
-                        w[k] = ptx::cvt_e4m3x2(p1, p0) | (ptx::cvt_e4m3x2(p3, p2) << 16);
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[8];
+                    if (!need_mask) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int e0 = 32 * q + 4 * k;
+                            float x0, x1, x2, x3;
+                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[e0], s[e0 + 1]), c2, b2), x0, x1);
+                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[e0 + 2], s[e0 + 3]), c2, b2), x2, x3);
+                            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
+                            acc0 = ptx::fadd2(acc0, ptx::f2pack(p0, p1));
+                            acc1 = ptx::fadd2(acc1, ptx::f2pack(p2, p3));
+                            w[k] = ptx::cvt_e4m3x2(p1, p0) | (ptx::cvt_e4m3x2(p3, p2) << 16);
+                        }
+                        ptx::tmem_st8(pcol + 8 * q, w);
+                    } else {
+                        // two E4M3 terms: P_hi = e4m3(p) in columns [0,32), P_lo = e4m3(p - P_hi) in [32,64)
+                        uint32_t wl[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int e0 = 32 * q + 4 * k;
+                            float pv[4];
+                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[e0], s[e0 + 1]), c2, b2), pv[0], pv[1]);
+                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[e0 + 2], s[e0 + 3]), c2, b2), pv[2], pv[3]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) pv[e] = ptx::ex2(pv[e]);
+                            acc0 = ptx::fadd2(acc0, ptx::f2pack(pv[0], pv[1]));
+                            acc1 = ptx::fadd2(acc1, ptx::f2pack(pv[2], pv[3]));
+                            const uint32_t h01 = ptx::cvt_e4m3x2(pv[1], pv[0]);
+                            const uint32_t h23 = ptx::cvt_e4m3x2(pv[3], pv[2]);
+                            float q0, q1, q2, q3;
+                            ptx::e4m3x2_to_f32(h01, q0, q1);
+                            ptx::e4m3x2_to_f32(h23, q2, q3);
+                            w[k] = h01 | (h23 << 16);
+                            wl[k] = ptx::cvt_e4m3x2(pv[1] - q1, pv[0] - q0) |
+                                    (ptx::cvt_e4m3x2(pv[3] - q3, pv[2] - q2) << 16);
+                        }
+                        ptx::tmem_st8(pcol + 8 * q, w);
+                        ptx::tmem_st8(pcol + 32 + 8 * q, wl);
                     }
-                    ptx::tmem_st32(tmem + lane_base + C::TM_S + sb * 128, w);
-                } else {
-                    // two E4M3 terms: P_hi = e4m3(p) in columns [0,32), P_lo = e4m3(p - P_hi) in [32,64)
-                    uint32_t wl[32];
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        float pv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) pv[e] = ptx::ex2(fmaf(s[4 * k + e], c, bias));
-                        sum += (pv[0] + pv[1]) + (pv[2] + pv[3]);
-                        const uint32_t h01 = ptx::cvt_e4m3x2(pv[1], pv[0]);
-                        const uint32_t h23 = ptx::cvt_e4m3x2(pv[3], pv[2]);
-                        float q0, q1, q2, q3;
-                        ptx::e4m3x2_to_f32(h01, q0, q1);
-                        ptx::e4m3x2_to_f32(h23, q2, q3);
-                        w[k] = h01 | (h23 << 16);
-                        wl[k] = ptx::cvt_e4m3x2(pv[1] - q1, pv[0] - q0) | (ptx::cvt_e4m3x2(pv[3] - q3, pv[2] - q2) << 16);
-                    }
-                    ptx::tmem_st32(tmem + lane_base + C::TM_S + sb * 128, w);
-                    ptx::tmem_st32(tmem + lane_base + C::TM_S + sb * 128 + 32, wl);
                 }
                 ptx::tmem_wait_st();
-                row_sum += sum;
+                float a0, a1, a2, a3;
+                ptx::f2unpack(acc0, a0, a1);
+                ptx::f2unpack(acc1, a2, a3);
+                row_sum += (a0 + a1) + (a2 + a3);
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(BAR(C::B_PF + sb));
@@ -654,7 +692,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
         }
         ptx::named_bar_sync(1, 256);
-    } else {
+      } else {
         // ======================================================== correction (warps 4-7)
         const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
         const bool warp_active = __any_sync(0xffffffffu, row_ok);
@@ -669,22 +707,47 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_arrive(BAR(C::B_AE + (it & 1)));
 #pragma unroll
             for (int c = 0; c < C::NPV; ++c) {
-                if (!W.wait_warp(BAR(C::B_OF), (uint32_t)pv_uses & 1u)) { ok = false; break; }
+                const int ob = pv_uses % C::NOT;
+                if (!W.wait_warp(BAR(C::B_OF + ob), (uint32_t)(pv_uses / C::NOT) & 1u)) { ok = false; break; }
                 ptx::tc_fence_after();
+                const uint32_t otile = tmem + lane_base + C::TM_OT + ob * C::OTW;
                 if (warp_active) {
+                    if constexpr (C::O_REGS) {
+                        // two 32-column loads in flight, then a packed fold of 64 values
+                        const uint64_t a2 = ptx::f2pack(alpha, alpha);
 #pragma unroll
-                    for (int j = 0; j < C::OTW / 32; ++j) {
-                        uint32_t u[32];
-                        ptx::tmem_ld32(tmem + lane_base + C::TM_OT + 32 * j, u);
-                        if constexpr (C::O_REGS) {
+                        for (int j = 0; j < C::OTW / 32; j += 2) {
+                            uint32_t u0[32], u1[32];
+                            ptx::tmem_ld32(otile + 32 * j, u0);
+                            if (j + 1 < C::OTW / 32) ptx::tmem_ld32(otile + 32 * (j + 1), u1);
                             ptx::tmem_wait_ld();
-                            ptx::reg_fence32(u);
+                            ptx::reg_fence32(u0);
+                            if (j + 1 < C::OTW / 32) ptx::reg_fence32(u1);
+                            const int nh = (j + 1 < C::OTW / 32) ? 2 : 1;
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const int idx = (C::O_REGS ? (c * C::OTW + 32 * j + i) : 0);
-                                o[idx] = (it == 0) ? u2f(u[i]) : fmaf(o[idx], alpha, u2f(u[i]));
+                            for (int h = 0; h < 2; ++h) {
+                                if (h < nh) {
+                                    const uint32_t *u = h ? u1 : u0;
+#pragma unroll
+                                    for (int i = 0; i < 32; i += 2) {
+                                        const int idx = (C::O_REGS ? (32 * (j + h) + i) : 0);
+                                        if (it == 0) {
+                                            o[idx] = u2f(u[i]);
+                                            o[idx + 1] = u2f(u[i + 1]);
+                                        } else {
+                                            const uint64_t r2 = ptx::ffma2(ptx::f2pack(o[idx], o[idx + 1]), a2,
+                                                                           ptx::f2pack(u2f(u[i]), u2f(u[i + 1])));
+                                            ptx::f2unpack(r2, o[idx], o[idx + 1]);
+                                        }
+                                    }
+                                }
                             }
-                        } else {
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < C::OTW / 32; ++j) {
+                            uint32_t u[32];
+                            ptx::tmem_ld32(otile + 32 * j, u);
                             const uint32_t orun = tmem + lane_base + C::TM_OR + c * C::OTW + 32 * j;
                             uint32_t v[32];
                             if (it > 0) {
@@ -706,7 +769,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(BAR(C::B_OE));
+                ptx::mbar_arrive(BAR(C::B_OE + ob));
                 ++pv_uses;
             }
         }
@@ -771,6 +834,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
             }
         }
+    }
     }
     // ------------------------------------------------------------ teardown
     ptx::tc_fence_before();
