@@ -51,17 +51,22 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _sources() + _headers() + [__file__])
 
 
-def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None) -> str:
-    if not force and not ptxas_verbose and up_to_date():
+def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None,
+          out_dir: str | None = None, defines=()) -> str:
+    """Compiles csrc/*.cu and links libfa8.so into ``out_dir`` (default: the in-tree
+    _build/); ``defines`` are extra -D macros (e.g. FA8_TRACE for the pipeline trace)."""
+    build_dir = out_dir or BUILD
+    lib = os.path.join(build_dir, "libfa8.so")
+    if not force and not ptxas_verbose and not defines and out_dir is None and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     srcs = _sources()
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(build_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
 
     def one(pair):
         src, obj = pair
-        cmd = [cc, "-c", src, "-o", obj] + _flags(ptxas_verbose)
+        cmd = [cc, "-c", src, "-o", obj] + _flags(ptxas_verbose) + [f"-D{d}" for d in defines]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, r.returncode, r.stdout + r.stderr
 
@@ -72,15 +77,15 @@ def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = N
             logs.append(f"== {os.path.basename(src)}\n{out}")
             if rc != 0:
                 raise RuntimeError(f"nvcc failed on {src}:\n{out}")
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+    with open(os.path.join(build_dir, "ptxas.log"), "w") as f:
         f.write("\n".join(logs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -56,6 +56,7 @@ namespace {
 
 thread_local std::string g_last_error;
 unsigned long long g_timeout_ns = 2000000000ull;
+unsigned long long *g_trace = nullptr;  // pipeline trace buffer (FA8_TRACE builds)
 
 fa8_status fail(fa8_status s, const char *fmt, ...) {
     char buf[512];
@@ -410,6 +411,20 @@ fa8_status fa8_check(void *stream) {
     return FA8_SUCCESS;
 }
 
+fa8_status fa8_debug_set_trace_buffer(void *device_buffer, size_t bytes) {
+    g_last_error.clear();
+#ifdef FA8_TRACE
+    const size_t need = sizeof(unsigned long long) * fa8::kTraceCtas * fa8::kTraceEvents * fa8::kTraceTiles;
+    if (device_buffer && bytes < need) return fail(FA8_ERR_INVALID_ARG, "trace buffer needs %zu bytes", need);
+    g_trace = static_cast<unsigned long long *>(device_buffer);
+    return FA8_SUCCESS;
+#else
+    (void)device_buffer;
+    (void)bytes;
+    return fail(FA8_ERR_UNSUPPORTED, "library built without FA8_TRACE");
+#endif
+}
+
 fa8_status fa8_debug_wait_probe(void *stream) {
     g_last_error.clear();
     DeviceState *ds = nullptr;
@@ -604,6 +619,7 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
     }
     p.timeout_ns = g_timeout_ns;
     p.status = ds->status;
+    p.trace = g_trace;
 
     const dim3 grid((unsigned)pl.num_slots, (unsigned)(pl.Hkv * pl.splits), 1);
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -15,8 +15,9 @@
 //   S_t   = Q K_t^T                     tcgen05.mma kind::f8f6f4, fp32 in TMEM
 //   m     lazy running max: moved only when the tile max exceeds it by more than
 //         tau = 0.75 (log2 units), tau <= log2(448) - 8 so that P never clips
-//   P_t   = 2^(s*c - m + 8) -> E4M3 (c = softmax_scale * dq * dk * log2 e), stored
-//         in TMEM over the first 32 columns of S_t
+//   P_t   = 2^(s*c - m + 8) -> E4M3 (c = softmax_scale * dq * dk * log2 e), stored in
+//         TMEM over S_t: the packed P of keys [32k, 32k+32) goes to column 32k of the S_t
+//         buffer (8 columns), after that 32-column slice of S_t has been read
 //   O_t   = P_t V_t                     accumulated from zero for every tile
 //         (on tiles that need a mask, P_t = P_hi + P_lo with P_lo = e4m3(p - P_hi) and
 //          both terms go through the PV MMA: rows with only a few visible keys keep
@@ -37,14 +38,29 @@ namespace fa8 {
 constexpr int kTileM = 128;     // Q rows per CTA = TMEM lanes
 constexpr int kTileN = 128;     // keys per KV tile
 constexpr int kNumThreads = 384;
-constexpr int kRegsMath = 224;  // softmax and correction warpgroups after setmaxnreg
-constexpr int kRegsCtl = 48;    // producer / MMA warpgroup (128 x 48 + 256 x 224 <= 384 x 168)
+constexpr int kRegsMath = 232;  // softmax and correction warpgroups after setmaxnreg
+constexpr int kRegsCtl = 32;    // producer / MMA warpgroup (128 x 32 + 256 x 232 <= 384 x 168)
 constexpr float kTau = 0.75f;   // lazy-rescale threshold, log2 units
 constexpr float kPBias = 8.0f;  // P carries a factor 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 enum : unsigned { kStatusTimeout = 1u, kStatusBounds = 2u };
+
+// Pipeline event trace (compiled in only with -DFA8_TRACE): clock64() per (CTA, event, tile)
+// for the first kTraceCtas CTAs of grid row 0; layout [cta][event][tile].
+constexpr int kTraceCtas = 8, kTraceEvents = 16, kTraceTiles = 64;
+#ifdef FA8_TRACE
+#define FA8_EV(ev, it)                                                                            \
+    do {                                                                                          \
+        if (p.trace && blockIdx.y == 0 && blockIdx.x < kTraceCtas && (it) < kTraceTiles)          \
+            p.trace[((size_t)blockIdx.x * kTraceEvents + (ev)) * kTraceTiles + (it)] = clock64(); \
+    } while (0)
+#else
+#define FA8_EV(ev, it) \
+    do {               \
+    } while (0)
+#endif
 
 struct FwdParams {
     int B, Hq, Hkv, G, rows_per_tile, pos_per_tile;
@@ -73,6 +89,7 @@ struct FwdParams {
     float *o_part, *lse_part;
     unsigned long long timeout_ns;
     unsigned int *status;
+    unsigned long long *trace;  // event timestamps (builds with FA8_TRACE only), may be null
 };
 
 struct CombineParams {
@@ -164,24 +181,30 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn_major)
 
 // Bounded mbarrier waits: give up when another role aborted or after timeout_ns, setting
 // the CTA abort flag and the device status word.
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+                                       unsigned long long timeout, unsigned int *status) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (ptx::globaltimer() - t0 > timeout) {
+            *abort = 1;
+            atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
 struct Waiter {
     volatile int *abort;
     unsigned long long timeout;
     unsigned int *status;
+    // fast path first; the bounded spin only when the phase is not complete yet
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
         if (ptx::mbar_try_wait(bar, parity)) return true;
-        const uint64_t t0 = ptx::globaltimer();
-        while (true) {
-#pragma unroll 1
-            for (int i = 0; i < 32; ++i)
-                if (ptx::mbar_try_wait(bar, parity)) return true;
-            if (*abort) return false;
-            if (ptx::globaltimer() - t0 > timeout) {
-                *abort = 1;
-                atomicOr(status, kStatusTimeout);
-                return false;
-            }
-        }
+        return wait_slow(bar, parity, abort, timeout, status);
     }
     // Whole-warp form: every lane waits, the result is made warp-uniform and the warp is
     // reconverged (needed before the warp-collective tcgen05.ld/st that follow).
@@ -404,6 +427,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Waiter W{abort_flag, p.timeout_ns, p.status};
+    if (tid == 0) FA8_EV(15, 0);
 
     if (warp >= 8) {
       ptx::setmaxnreg_dec<kRegsCtl>();
@@ -440,6 +464,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int c3 = p.kv_mode == 1 ? 0 : b;
             // K tile
             if (!W.wait_warp(BAR(C::B_KE + st), ph ^ 1u)) break;
+            if (lane == 0) FA8_EV(0, it);
             if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_KF + st), (uint32_t)C::K_BYTES);
             __syncwarp();
             const uint32_t dK = sK + st * C::K_BYTES;
@@ -458,6 +483,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             issued_k = it + 1;
             // V tile
             if (!W.wait_warp(BAR(C::B_VE + st), ph ^ 1u)) break;
+            if (lane == 0) FA8_EV(1, it);
             if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_VF + st), (uint32_t)C::V_BYTES);
             __syncwarp();
             const uint32_t dV = sV + st * C::V_BYTES;
@@ -497,7 +523,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const int sb = j % C::NS;
                 const int vs = j % C::STAGES;
                 if (!W.wait(BAR(C::B_PF + sb), (uint32_t)(j / C::NS) & 1u)) return false;
+                FA8_EV(10, j);
                 if (!W.wait(BAR(C::B_VF + vs), (uint32_t)(j / C::STAGES) & 1u)) return false;
+                FA8_EV(11, j);
                 ptx::tc_fence_after();
                 const uint32_t vbase = sV + vs * C::V_BYTES;
                 const bool two_term = tile_needs_mask((t_beg + j) * kTileN, Lk, p.causal, p.window_left, pos0,
@@ -507,19 +535,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const int ob = pv_uses % C::NOT;
                     const uint32_t otile = tmem + C::TM_OT + ob * C::OTW;
                     if (!W.wait(BAR(C::B_OE + ob), ((uint32_t)(pv_uses / C::NOT) & 1u) ^ 1u)) return false;
+                    FA8_EV(12, j);
                     ptx::tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kTileN / 32; ++kk) {
-                        const uint32_t a = tmem + C::TM_S + sb * 128 + kk * 8;
+                        const uint32_t a = tmem + C::TM_S + sb * 128 + kk * 32;
                         const uint64_t bd =
                             sdesc(vbase + (c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV,
                                   C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
                         ptx::mma_f8_ts(otile, a, bd, kIdescPV, kk > 0 ? 1u : 0u);
                     }
-                    if (two_term) {  // + P_lo V (P_lo in the next 32 columns)
+                    if (two_term) {  // + P_lo V (P_lo 8 columns after each P_hi slice)
 #pragma unroll
                         for (int kk = 0; kk < kTileN / 32; ++kk) {
-                            const uint32_t a = tmem + C::TM_S + sb * 128 + 32 + kk * 8;
+                            const uint32_t a = tmem + C::TM_S + sb * 128 + kk * 32 + 8;
                             const uint64_t bd =
                                 sdesc(vbase + (c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV,
                                       C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
@@ -530,11 +559,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     ++pv_uses;
                 }
                 ptx::tc_commit(BAR(C::B_VE + vs));
+                FA8_EV(3, j);
                 return true;
             };
             for (int it = 0; ok && it < n_tiles; ++it) {
                 const int ks = it % C::STAGES;
                 if (!W.wait(BAR(C::B_KF + ks), (uint32_t)(it / C::STAGES) & 1u)) { ok = false; break; }
+                FA8_EV(9, it);
                 ptx::tc_fence_after();
                 if (C::NS == 1 && it > 0 && !do_pv(it - 1)) { ok = false; break; }
                 const int sb = it % C::NS;
@@ -549,6 +580,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 ptx::tc_commit(BAR(C::B_SF + sb));
                 ptx::tc_commit(BAR(C::B_KE + ks));
+                FA8_EV(2, it);
                 if (C::NS == 2 && it > 0 && !do_pv(it - 1)) { ok = false; break; }
             }
             if (ok) ok = do_pv(n_tiles - 1);
@@ -576,36 +608,53 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int k0 = (t_beg + it) * kTileN;
             const int sb = it % C::NS;
             if (!W.wait_warp(BAR(C::B_SF + sb), (uint32_t)(it / C::NS) & 1u)) break;
+            if (tid == 0) FA8_EV(4, it);
             ptx::tc_fence_after();
             float alpha = 1.f;
             if (warp_active) {
-                uint32_t u[4][32];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) ptx::tmem_ld32(tmem + lane_base + C::TM_S + sb * 128 + 32 * j, u[j]);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 4; ++j) ptx::reg_fence32(u[j]);
-                float s[128];
-#pragma unroll
-                for (int i = 0; i < 128; ++i) s[i] = u2f(u[i >> 5][i & 31]);
+                const uint32_t scol = tmem + lane_base + C::TM_S + sb * 128;
                 const bool need_mask = tile_needs_mask(k0, Lk, p.causal, p.window_left, pos0, pos_last, delta);
-                if (need_mask) {
-                    const int hi = hi_row - k0, lo = lo_row - k0;
+                const int hi = hi_row - k0, lo = lo_row - k0;  // visible keys of this row: [lo, hi]
+                // ---- pass 1: row max of the tile
+                float mx;
+                if (!need_mask) {
+                    uint32_t u[4][32];
 #pragma unroll
-                    for (int i = 0; i < 128; ++i)
-                        if (i > hi || i < lo) s[i] = -INFINITY;
+                    for (int j = 0; j < 4; ++j) ptx::tmem_ld32(scol + 32 * j, u[j]);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) ptx::reg_fence32(u[j]);
+                    float mq[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint32_t *v = &u[q >> 1][(q & 1) * 16];
+                        float m = ptx::fmax3(u2f(v[0]), u2f(v[1]), u2f(v[2]));
+#pragma unroll
+                        for (int i = 3; i < 15; i += 2) m = ptx::fmax3(m, u2f(v[i]), u2f(v[i + 1]));
+                        mq[q] = fmaxf(m, u2f(v[15]));
+                    }
+                    mx = fmaxf(ptx::fmax3(mq[0], mq[1], mq[2]),
+                               ptx::fmax3(ptx::fmax3(mq[3], mq[4], mq[5]), mq[6], mq[7]));
+                } else {
+                    mx = -INFINITY;
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t u[32];
+                        ptx::tmem_ld32(scol + 32 * q, u);
+                        ptx::tmem_wait_ld();
+                        ptx::reg_fence32(u);
+                        float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            const int key0 = 32 * q + i;
+                            const float x0 = (key0 > hi || key0 < lo) ? -INFINITY : u2f(u[i]);
+                            const float x1 = (key0 + 1 > hi || key0 + 1 < lo) ? -INFINITY : u2f(u[i + 1]);
+                            m0 = fmaxf(m0, x0);
+                            m1 = fmaxf(m1, x1);
+                        }
+                        mx = ptx::fmax3(mx, m0, m1);
+                    }
                 }
-                // row max: eight independent three-input chains of 16, then a small tree
-                float mq[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float m = ptx::fmax3(s[16 * q], s[16 * q + 1], s[16 * q + 2]);
-#pragma unroll
-                    for (int i = 3; i < 15; i += 2) m = ptx::fmax3(m, s[16 * q + i], s[16 * q + i + 1]);
-                    mq[q] = fmaxf(m, s[16 * q + 15]);
-                }
-                const float mx = fmaxf(ptx::fmax3(mq[0], mq[1], mq[2]),
-                                       ptx::fmax3(ptx::fmax3(mq[3], mq[4], mq[5]), mq[6], mq[7]));
                 const float mt = mx * c;
                 if (mt > m_run + kTau) {
                     alpha = ptx::ex2(m_run - mt);
@@ -615,48 +664,54 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
                 const uint64_t b2 = ptx::f2pack(bias, bias);
                 uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
-                const uint32_t pcol = tmem + lane_base + C::TM_S + sb * 128;
-                // P in four chunks of 32 keys (8 TMEM columns of packed E4M3 each)
+                // ---- pass 2: P = 2^(s c - m + 8), two 32-key slices per step
+#pragma unroll 1
+                for (int qq = 0; qq < 4; qq += 2) {
+                    uint32_t u[2][32];
+                    ptx::tmem_ld32(scol + 32 * qq, u[0]);
+                    ptx::tmem_ld32(scol + 32 * qq + 32, u[1]);
+                    ptx::tmem_wait_ld();
+                    ptx::reg_fence32(u[0]);
+                    ptx::reg_fence32(u[1]);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t w[8];
-                    if (!need_mask) {
+                    for (int h = 0; h < 2; ++h) {
+                        const int kb = 32 * (qq + h);  // first key of this slice
+                        float x[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) x[i] = u2f(u[h][i]);
+                        if (need_mask) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (kb + i > hi || kb + i < lo) x[i] = -INFINITY;
+                        }
+                        uint32_t w[8];
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
-                            const int e0 = 32 * q + 4 * k;
                             float x0, x1, x2, x3;
-                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[e0], s[e0 + 1]), c2, b2), x0, x1);
-                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[e0 + 2], s[e0 + 3]), c2, b2), x2, x3);
-                            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
-                            acc0 = ptx::fadd2(acc0, ptx::f2pack(p0, p1));
-                            acc1 = ptx::fadd2(acc1, ptx::f2pack(p2, p3));
-                            w[k] = ptx::cvt_e4m3x2(p1, p0) | (ptx::cvt_e4m3x2(p3, p2) << 16);
+                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(x[4 * k], x[4 * k + 1]), c2, b2), x0, x1);
+                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(x[4 * k + 2], x[4 * k + 3]), c2, b2), x2, x3);
+                            x[4 * k] = ptx::ex2(x0);
+                            x[4 * k + 1] = ptx::ex2(x1);
+                            x[4 * k + 2] = ptx::ex2(x2);
+                            x[4 * k + 3] = ptx::ex2(x3);
+                            acc0 = ptx::fadd2(acc0, ptx::f2pack(x[4 * k], x[4 * k + 1]));
+                            acc1 = ptx::fadd2(acc1, ptx::f2pack(x[4 * k + 2], x[4 * k + 3]));
+                            w[k] = ptx::cvt_e4m3x2(x[4 * k + 1], x[4 * k]) |
+                                   (ptx::cvt_e4m3x2(x[4 * k + 3], x[4 * k + 2]) << 16);
                         }
-                        ptx::tmem_st8(pcol + 8 * q, w);
-                    } else {
-                        // two E4M3 terms: P_hi = e4m3(p) in columns [0,32), P_lo = e4m3(p - P_hi) in [32,64)
-                        uint32_t wl[8];
+                        ptx::tmem_st8(scol + kb, w);
+                        if (need_mask) {
+                            // second E4M3 term on masked tiles: P_lo = e4m3(p - P_hi)
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const int e0 = 32 * q + 4 * k;
-                            float pv[4];
-                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[e0], s[e0 + 1]), c2, b2), pv[0], pv[1]);
-                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[e0 + 2], s[e0 + 3]), c2, b2), pv[2], pv[3]);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) pv[e] = ptx::ex2(pv[e]);
-                            acc0 = ptx::fadd2(acc0, ptx::f2pack(pv[0], pv[1]));
-                            acc1 = ptx::fadd2(acc1, ptx::f2pack(pv[2], pv[3]));
-                            const uint32_t h01 = ptx::cvt_e4m3x2(pv[1], pv[0]);
-                            const uint32_t h23 = ptx::cvt_e4m3x2(pv[3], pv[2]);
-                            float q0, q1, q2, q3;
-                            ptx::e4m3x2_to_f32(h01, q0, q1);
-                            ptx::e4m3x2_to_f32(h23, q2, q3);
-                            w[k] = h01 | (h23 << 16);
-                            wl[k] = ptx::cvt_e4m3x2(pv[1] - q1, pv[0] - q0) |
-                                    (ptx::cvt_e4m3x2(pv[3] - q3, pv[2] - q2) << 16);
+                            for (int k = 0; k < 8; ++k) {
+                                float q0, q1, q2, q3;
+                                ptx::e4m3x2_to_f32(w[k] & 0xFFFFu, q0, q1);
+                                ptx::e4m3x2_to_f32(w[k] >> 16, q2, q3);
+                                w[k] = ptx::cvt_e4m3x2(x[4 * k + 1] - q1, x[4 * k] - q0) |
+                                       (ptx::cvt_e4m3x2(x[4 * k + 3] - q3, x[4 * k + 2] - q2) << 16);
+                            }
+                            ptx::tmem_st8(scol + kb + 8, w);
                         }
-                        ptx::tmem_st8(pcol + 8 * q, w);
-                        ptx::tmem_st8(pcol + 32 + 8 * q, wl);
                     }
                 }
                 ptx::tmem_wait_st();
@@ -667,9 +722,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(BAR(C::B_PF + sb));
+            if (tid == 0) FA8_EV(5, it);
             if (!W.wait_warp(BAR(C::B_AE + (it & 1)), ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
             alpha_ring[(it & 1) * 128 + r] = alpha;
             ptx::mbar_arrive(BAR(C::B_AF + (it & 1)));
+            if (tid == 0) FA8_EV(6, it);
         }
         // finalize: the 2^8 bias cancels between O and row_sum and is removed from the LSE
         float scale_o = 0.f, lse;
@@ -709,38 +766,27 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             for (int c = 0; c < C::NPV; ++c) {
                 const int ob = pv_uses % C::NOT;
                 if (!W.wait_warp(BAR(C::B_OF + ob), (uint32_t)(pv_uses / C::NOT) & 1u)) { ok = false; break; }
+                if (tid == 128 && c == 0) FA8_EV(7, it);
                 ptx::tc_fence_after();
                 const uint32_t otile = tmem + lane_base + C::TM_OT + ob * C::OTW;
                 if (warp_active) {
                     if constexpr (C::O_REGS) {
-                        // two 32-column loads in flight, then a packed fold of 64 values
+                        // one 32-column slice at a time, packed fold
                         const uint64_t a2 = ptx::f2pack(alpha, alpha);
 #pragma unroll
-                        for (int j = 0; j < C::OTW / 32; j += 2) {
-                            uint32_t u0[32], u1[32];
-                            ptx::tmem_ld32(otile + 32 * j, u0);
-                            if (j + 1 < C::OTW / 32) ptx::tmem_ld32(otile + 32 * (j + 1), u1);
+                        for (int j = 0; j < C::OTW / 32; ++j) {
+                            uint32_t u[32];
+                            ptx::tmem_ld32(otile + 32 * j, u);
                             ptx::tmem_wait_ld();
-                            ptx::reg_fence32(u0);
-                            if (j + 1 < C::OTW / 32) ptx::reg_fence32(u1);
-                            const int nh = (j + 1 < C::OTW / 32) ? 2 : 1;
+                            ptx::reg_fence32(u);
 #pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                if (h < nh) {
-                                    const uint32_t *u = h ? u1 : u0;
-#pragma unroll
-                                    for (int i = 0; i < 32; i += 2) {
-                                        const int idx = (C::O_REGS ? (32 * (j + h) + i) : 0);
-                                        if (it == 0) {
-                                            o[idx] = u2f(u[i]);
-                                            o[idx + 1] = u2f(u[i + 1]);
-                                        } else {
-                                            const uint64_t r2 = ptx::ffma2(ptx::f2pack(o[idx], o[idx + 1]), a2,
-                                                                           ptx::f2pack(u2f(u[i]), u2f(u[i + 1])));
-                                            ptx::f2unpack(r2, o[idx], o[idx + 1]);
-                                        }
-                                    }
-                                }
+                            for (int i = 0; i < 32; i += 2) {
+                                // O starts at 0 and the first visible tile has alpha = 0,
+                                // so no first-tile special case is needed
+                                const int idx = (C::O_REGS ? (32 * j + i) : 0);
+                                const uint64_t r2 = ptx::ffma2(ptx::f2pack(o[idx], o[idx + 1]), a2,
+                                                               ptx::f2pack(u2f(u[i]), u2f(u[i + 1])));
+                                ptx::f2unpack(r2, o[idx], o[idx + 1]);
                             }
                         }
                     } else {
@@ -770,6 +816,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(BAR(C::B_OE + ob));
+                if (tid == 128 && c == C::NPV - 1) FA8_EV(8, it);
                 ++pv_uses;
             }
         }
@@ -839,6 +886,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // ------------------------------------------------------------ teardown
     ptx::tc_fence_before();
     __syncthreads();
+    if (tid == 0) FA8_EV(15, 1);
     if (warp == 9) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::TM_COLS);

@@ -15,7 +15,8 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libfa8.so")
+# FA8_LIBRARY may point at another build of the same library (e.g. one with FA8_TRACE)
+LIB_PATH = os.environ.get("FA8_LIBRARY") or os.path.join(_HERE, "_build", "libfa8.so")
 
 FA8_SUCCESS = 0
 FA8_ERR_INVALID_ARG = 1
@@ -57,6 +58,7 @@ SIGNATURES = {
     "fa8_check": (ctypes.c_int, [ctypes.c_void_p]),
     "fa8_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "fa8_debug_wait_probe": (ctypes.c_int, [ctypes.c_void_p]),
+    "fa8_debug_set_trace_buffer": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t]),
     "fa8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa8_last_error": (ctypes.c_char_p, []),
     "fa8_version": (ctypes.c_int, []),

@@ -156,6 +156,15 @@ FA8_API fa8_status fa8_set_wait_timeout_ns(uint64_t ns);
  */
 FA8_API fa8_status fa8_debug_wait_probe(void *stream);
 
+/*
+ * fa8_debug_set_trace_buffer -- in a library built with -DFA8_TRACE, later forward launches
+ * record clock64() at each pipeline event (TMA issue, MMA issue, softmax and fold
+ * hand-offs) of the first 8 CTAs into `device_buffer`, laid out [cta 8][event 16][tile 64]
+ * as uint64 (needs 65536 bytes); NULL turns it off.  Other builds return
+ * FA8_ERR_UNSUPPORTED.  Intended for pipeline tuning, not for production use.
+ */
+FA8_API fa8_status fa8_debug_set_trace_buffer(void *device_buffer, size_t bytes);
+
 FA8_API const char *fa8_status_string(fa8_status s);
 /* Reason for the last error returned on the calling thread ("" if none). */
 FA8_API const char *fa8_last_error(void);
