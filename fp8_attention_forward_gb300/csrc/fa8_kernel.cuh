@@ -233,12 +233,13 @@ __device__ __forceinline__ bool tile_needs_mask(int k0, int Lk, int causal, int 
            (window_left >= 0 && k0 < pos_last + delta - window_left);
 }
 
-// Maps a varlen grid slot to (request, m-block): the slots enumerate each request's
-// m-blocks in order; within a request the m-block order is reversed so that, with a
-// causal mask, the longer rows start first.  Whole warp must call it.
-__device__ __forceinline__ bool varlen_slot(const FwdParams &p, int x, int &b, int &mb) {
+// Maps a varlen grid slot to (request, slot within the request): the slots enumerate each
+// request's groups of `per_slot` consecutive m-blocks in order; within a request the order
+// is reversed so that, with a causal mask, the longer rows start first.  Whole warp must
+// call it.
+__device__ __forceinline__ bool varlen_slot(const FwdParams &p, int x, int &b, int &mb, int per_slot = 1) {
     const int lane = threadIdx.x & 31;
-    const int P = p.pos_per_tile;
+    const int P = p.pos_per_tile * per_slot;
     int base = 0;
     for (int s0 = 0; s0 < p.B; s0 += 32) {
         const int s = s0 + lane;
@@ -522,6 +523,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             auto do_pv = [&](int j) -> bool {
                 const int sb = j % C::NS;
                 const int vs = j % C::STAGES;
+                FA8_EV(13, j);
                 if (!W.wait(BAR(C::B_PF + sb), (uint32_t)(j / C::NS) & 1u)) return false;
                 FA8_EV(10, j);
                 if (!W.wait(BAR(C::B_VF + vs), (uint32_t)(j / C::STAGES) & 1u)) return false;
@@ -578,6 +580,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     const uint64_t kd = sdesc(kbase + chunk * C::CHUNK_K + off, 16, 8 * C::CW, swz_layout(C::CW));
                     ptx::mma_f8_ss(tmem + C::TM_S + sb * 128, qd, kd, kIdescQK, kk > 0 ? 1u : 0u);
                 }
+                FA8_EV(14, it);
                 ptx::tc_commit(BAR(C::B_SF + sb));
                 ptx::tc_commit(BAR(C::B_KE + ks));
                 FA8_EV(2, it);
