@@ -164,7 +164,6 @@ struct Plan {
     int splits = 1;
     long long max_lk = 0;
     size_t ws_bytes = 0;
-    int two_tile = 0;  // prefill kernel: two Q tiles per CTA
 };
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -275,14 +274,8 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
     }
     if (cu_k && (st = check_int_vec(cu_k, "cu_seqlens_k", p.B + 1))) return st;
 
-    // ---- kernel form, grid and splits (shapes and SM count only: safe under graph capture).
-    // Requests with more than one 128-row Q tile per kv-head on average (prefill) use the
-    // two-Q-tile kernel when its O fits in registers (dv <= 128); decode-shaped problems use
-    // one Q tile per CTA.
-    const double avg_rows = (p.q_varlen ? (double)p.total_q / p.B : (double)p.Sq) * p.G;
-    p.two_tile = (p.DV <= 128 && avg_rows > 128.0) ? 1 : 0;
-    const int per_slot = p.two_tile ? 2 : 1;
-    const long long pos_per_slot = (long long)p.P * per_slot;
+    // ---- grid and splits (shapes and SM count only: safe under graph capture)
+    const long long pos_per_slot = p.P;
     if (p.q_varlen) {
         p.num_slots = ((long long)p.total_q + pos_per_slot - 1) / pos_per_slot + p.B;
     } else {
@@ -633,15 +626,12 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
     const dim3 grid((unsigned)pl.num_slots, (unsigned)(pl.Hkv * pl.splits), 1);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    switch (pl.D * 1000 + pl.DV + (pl.two_tile ? 1000000 : 0)) {
+    switch (pl.D * 1000 + pl.DV) {
         case 64064: e = fa8::launch_fwd<64, 64>(p, tq, tk, tv, grid, s); break;
         case 128128: e = fa8::launch_fwd<128, 128>(p, tq, tk, tv, grid, s); break;
         case 192128: e = fa8::launch_fwd<192, 128>(p, tq, tk, tv, grid, s); break;
         case 192192: e = fa8::launch_fwd<192, 192>(p, tq, tk, tv, grid, s); break;
         case 256256: e = fa8::launch_fwd<256, 256>(p, tq, tk, tv, grid, s); break;
-        case 1064064: e = fa8::launch_fwd2<64, 64>(p, tq, tk, tv, grid, s); break;
-        case 1128128: e = fa8::launch_fwd2<128, 128>(p, tq, tk, tv, grid, s); break;
-        case 1192128: e = fa8::launch_fwd2<192, 128>(p, tq, tk, tv, grid, s); break;
         default: return fail(FA8_ERR_UNSUPPORTED, "no kernel for (%d, %d)", pl.D, pl.DV);
     }
     if (e != cudaSuccess) return cuda_fail(e, "forward kernel launch");

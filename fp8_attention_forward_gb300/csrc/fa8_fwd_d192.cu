@@ -3,5 +3,4 @@
 namespace fa8 {
 FA8_DEFINE_FWD(192, 128)
 FA8_DEFINE_FWD(192, 192)
-FA8_DEFINE_FWD2(192, 128)
 }  // namespace fa8

@@ -3,12 +3,17 @@
 //
 // One CTA computes one 128-row Q tile: the rows are (query position, q-head) pairs of one
 // kv-head group, packed position-major (PackGQA), against the kv-head's keys, for one
-// split of the request's key range.  Roles (384 threads, three warpgroups):
-//   warps 0-3   softmax: thread r owns TMEM lane r = tile row r
-//   warps 4-7   correction: two-level PV fold into fp32 O, epilogue
-//   warp 8      TMA producer (Q once, K/V tiles into S-stage rings)
-//   warp 9      MMA issuer (lane 0) and TMEM owner
-//   warps 10-11 idle; the third warpgroup gives its registers to the first two
+// split of the request's key range.  Roles (512 threads, four warpgroups):
+//   warps 0-3   softmax, keys [0, 64) of every tile: thread r owns TMEM lane r = row r
+//   warps 4-7   softmax, keys [64, 128) of the same rows; the two halves exchange their
+//               row maxima once per tile and their row sums once at the end
+//   warps 8-11  correction: two-level PV fold into fp32 O, epilogue
+//   warp 12     TMA producer (Q once, K/V tiles into S-stage rings)
+//   warp 13     MMA issuer (lane 0) and TMEM owner
+//   warps 14-15 idle (the control warpgroup gives its registers to the correction)
+// Splitting each row over two warps halves the per-warp softmax work per tile, so the
+// softmax keeps pace with the tensor core; each half reads its 64 S columns from TMEM in a
+// single round trip per tile.
 //
 // Per 128-key tile t (sources: "[Cute,Fwd,Sm90] Native FP8 (E4M3 Q/K/V) forward for
 // Hopper", Design; "tml-fa4 PR #4", Summary and "Correctness fix over #1"):
@@ -37,9 +42,11 @@ namespace fa8 {
 
 constexpr int kTileM = 128;     // Q rows per CTA = TMEM lanes
 constexpr int kTileN = 128;     // keys per KV tile
-constexpr int kNumThreads = 384;
-constexpr int kRegsMath = 232;  // softmax and correction warpgroups after setmaxnreg
-constexpr int kRegsCtl = 32;    // producer / MMA warpgroup (128 x 32 + 256 x 232 <= 384 x 168)
+constexpr int kNumThreads = 512;
+// registers per thread after setmaxnreg; 256 x 112 + 128 x 240 + 128 x 48 = 512 x 128 (launch)
+constexpr int kRegsSoft = 112;
+constexpr int kRegsCorr = 240;
+constexpr int kRegsCtl = 48;
 constexpr float kTau = 0.75f;   // lazy-rescale threshold, log2 units
 constexpr float kPBias = 8.0f;  // P carries a factor 2^8
 constexpr float kLog2e = 1.4426950408889634f;
@@ -127,7 +134,7 @@ struct Cfg {
     static constexpr int Q_BYTES = kTileM * D;
     static constexpr int K_BYTES = kTileN * D;
     static constexpr int V_BYTES = kTileN * DV;
-    static constexpr int MISC_BYTES = 4096;
+    static constexpr int MISC_BYTES = 6144;
     static constexpr int SMEM_LIMIT = 232448;  // max dynamic smem per block on sm_103
     static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - MISC_BYTES - Q_BYTES) / (K_BYTES + V_BYTES);
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
@@ -148,7 +155,10 @@ struct Cfg {
     static constexpr int B_OE = B_OF + NOT;  // NOT slots
     static constexpr int B_AF = B_OE + NOT;  // 2 slots
     static constexpr int B_AE = B_AF + 2;  // 2 slots
-    static constexpr int B_DONE = B_AE + 2;
+    static constexpr int B_XCH = B_AE + 2;   // 2 slots: row-max exchange between the halves
+    static constexpr int B_SUM = B_XCH + 2;  // half 1 -> half 0: final partial row sums
+    static constexpr int B_FIN = B_SUM + 1;  // half 0 -> correction: final O scale
+    static constexpr int B_DONE = B_FIN + 1;
     static constexpr int NUM_BARS = B_DONE + 1;
     static_assert(STAGES >= 2, "smem too small for two K/V stages");
     static_assert(NUM_BARS * 8 <= 512, "barrier area");
@@ -385,6 +395,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 516);
     float *alpha_ring = reinterpret_cast<float *>(misc + 1024);  // [2][128]
     float *row_scale = reinterpret_cast<float *>(misc + 2048);   // [128]
+    float *mx_part = reinterpret_cast<float *>(misc + 2560);     // [2 parity][2 half][128]
+    float *sum_part = reinterpret_cast<float *>(misc + 4608);    // [128]
     const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
     const uint32_t sK = ptx::smem_u32(smem + C::OFF_K);
     const uint32_t sV = ptx::smem_u32(smem + C::OFF_V);
@@ -399,7 +411,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         for (int i = 0; i < C::NS; ++i) {
             ptx::mbar_init(BAR(C::B_SF + i), 1);
-            ptx::mbar_init(BAR(C::B_PF + i), 128);
+            ptx::mbar_init(BAR(C::B_PF + i), 256);
         }
         for (int i = 0; i < C::NOT; ++i) {
             ptx::mbar_init(BAR(C::B_OF + i), 1);
@@ -408,18 +420,21 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(BAR(C::B_AF + i), 128);
             ptx::mbar_init(BAR(C::B_AE + i), 128);
+            ptx::mbar_init(BAR(C::B_XCH + i), 256);
         }
+        ptx::mbar_init(BAR(C::B_SUM), 128);
+        ptx::mbar_init(BAR(C::B_FIN), 128);
         ptx::mbar_init(BAR(C::B_DONE), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == 12 && lane == 0) {
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
     }
-    if (warp == 9) {
+    if (warp == 13) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TM_COLS);
         ptx::tmem_relinquish();
     }
@@ -430,9 +445,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const Waiter W{abort_flag, p.timeout_ns, p.status};
     if (tid == 0) FA8_EV(15, 0);
 
-    if (warp >= 8) {
+    if (warp >= 12) {
       ptx::setmaxnreg_dec<kRegsCtl>();
-      if (warp == 8) {
+      if (warp == 12) {
         // ======================================================== TMA producer
         const bool paged = p.kv_mode == 2;
         int issued_k = 0, issued_v = 0;
@@ -512,7 +527,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 W.drain(BAR(C::B_VF + i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u);
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ======================================================== MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdescQK = idesc_e4m3(kTileM, kTileN, false);
@@ -593,71 +608,60 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         __syncwarp();
       }
-    } else {
-      ptx::setmaxnreg_inc<kRegsMath>();
-      if (warp < 4) {
-        // ======================================================== softmax
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    } else if (warp < 8) {
+      ptx::setmaxnreg_dec<kRegsSoft>();
+      {
+        // ======================================================== softmax (half h of each row)
+        const int h = warp >> 2;  // keys [64 h, 64 h + 64) of every tile
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const bool warp_active = __any_sync(0xffffffffu, row_ok);
         const float dqv = p.dq ? p.dq[b * p.dq_sb + kvh * p.dq_sh] : 1.f;
         const float dkv = p.dk ? p.dk[b * p.dk_sb + kvh * p.dk_sh] : 1.f;
-        const float dvv = p.dv ? p.dv[b * p.dv_sb + kvh * p.dv_sh] : 1.f;
         const float c = p.scale_log2 * dqv * dkv;
         const uint64_t c2 = ptx::f2pack(c, c);
         const int hi_row = p.causal ? min(Lk - 1, rpos + delta) : Lk - 1;
         const int lo_row = p.window_left >= 0 ? max(0, rpos + delta - p.window_left) : 0;
-        float m_run = -INFINITY, row_sum = 0.f;
+        float m_run = -INFINITY, row_sum = 0.f;  // identical m_run in both halves
         for (int it = 0; it < n_tiles; ++it) {
             const int k0 = (t_beg + it) * kTileN;
             const int sb = it % C::NS;
             if (!W.wait_warp(BAR(C::B_SF + sb), (uint32_t)(it / C::NS) & 1u)) break;
             if (tid == 0) FA8_EV(4, it);
             ptx::tc_fence_after();
+            const uint32_t scol = tmem + lane_base + C::TM_S + sb * 128 + 64 * h;
+            const bool need_mask = tile_needs_mask(k0, Lk, p.causal, p.window_left, pos0, pos_last, delta);
+            const int hi = hi_row - k0 - 64 * h, lo = lo_row - k0 - 64 * h;  // visible: [lo, hi]
+            uint32_t u[2][32];
+            float mh = -INFINITY;
+            if (warp_active) {
+                ptx::tmem_ld32(scol, u[0]);
+                ptx::tmem_ld32(scol + 32, u[1]);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence32(u[0]);
+                ptx::reg_fence32(u[1]);
+                if (need_mask) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        if (i > hi || i < lo) u[i >> 5][i & 31] = __float_as_uint(-INFINITY);
+                }
+                float mq[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t *v = &u[q >> 1][(q & 1) * 16];
+                    float m = ptx::fmax3(u2f(v[0]), u2f(v[1]), u2f(v[2]));
+#pragma unroll
+                    for (int i = 3; i < 15; i += 2) m = ptx::fmax3(m, u2f(v[i]), u2f(v[i + 1]));
+                    mq[q] = fmaxf(m, u2f(v[15]));
+                }
+                mh = fmaxf(ptx::fmax3(mq[0], mq[1], mq[2]), mq[3]);
+            }
+            // exchange the half-row maxima (double-buffered slots, bounded wait)
+            mx_part[((it & 1) * 2 + h) * 128 + r] = mh;
+            ptx::mbar_arrive(BAR(C::B_XCH + (it & 1)));
+            if (!W.wait_warp(BAR(C::B_XCH + (it & 1)), (uint32_t)(it >> 1) & 1u)) break;
+            const float mx = fmaxf(mh, mx_part[((it & 1) * 2 + (h ^ 1)) * 128 + r]);
             float alpha = 1.f;
             if (warp_active) {
-                const uint32_t scol = tmem + lane_base + C::TM_S + sb * 128;
-                const bool need_mask = tile_needs_mask(k0, Lk, p.causal, p.window_left, pos0, pos_last, delta);
-                const int hi = hi_row - k0, lo = lo_row - k0;  // visible keys of this row: [lo, hi]
-                // ---- pass 1: row max of the tile
-                float mx;
-                if (!need_mask) {
-                    uint32_t u[4][32];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) ptx::tmem_ld32(scol + 32 * j, u[j]);
-                    ptx::tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) ptx::reg_fence32(u[j]);
-                    float mq[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint32_t *v = &u[q >> 1][(q & 1) * 16];
-                        float m = ptx::fmax3(u2f(v[0]), u2f(v[1]), u2f(v[2]));
-#pragma unroll
-                        for (int i = 3; i < 15; i += 2) m = ptx::fmax3(m, u2f(v[i]), u2f(v[i + 1]));
-                        mq[q] = fmaxf(m, u2f(v[15]));
-                    }
-                    mx = fmaxf(ptx::fmax3(mq[0], mq[1], mq[2]),
-                               ptx::fmax3(ptx::fmax3(mq[3], mq[4], mq[5]), mq[6], mq[7]));
-                } else {
-                    mx = -INFINITY;
-#pragma unroll 1
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t u[32];
-                        ptx::tmem_ld32(scol + 32 * q, u);
-                        ptx::tmem_wait_ld();
-                        ptx::reg_fence32(u);
-                        float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            const int key0 = 32 * q + i;
-                            const float x0 = (key0 > hi || key0 < lo) ? -INFINITY : u2f(u[i]);
-                            const float x1 = (key0 + 1 > hi || key0 + 1 < lo) ? -INFINITY : u2f(u[i + 1]);
-                            m0 = fmaxf(m0, x0);
-                            m1 = fmaxf(m1, x1);
-                        }
-                        mx = ptx::fmax3(mx, m0, m1);
-                    }
-                }
                 const float mt = mx * c;
                 if (mt > m_run + kTau) {
                     alpha = ptx::ex2(m_run - mt);
@@ -667,54 +671,37 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
                 const uint64_t b2 = ptx::f2pack(bias, bias);
                 uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
-                // ---- pass 2: P = 2^(s c - m + 8), two 32-key slices per step
-#pragma unroll 1
-                for (int qq = 0; qq < 4; qq += 2) {
-                    uint32_t u[2][32];
-                    ptx::tmem_ld32(scol + 32 * qq, u[0]);
-                    ptx::tmem_ld32(scol + 32 * qq + 32, u[1]);
-                    ptx::tmem_wait_ld();
-                    ptx::reg_fence32(u[0]);
-                    ptx::reg_fence32(u[1]);
+                // P = 2^(s c - m + 8); the packed E4M3 of keys [32q, 32q+32) goes to column
+                // 32q of the S buffer (P_lo 8 columns later on masked tiles)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int kb = 32 * (qq + h);  // first key of this slice
-                        float x[32];
+                for (int g = 0; g < 2; ++g) {
+                    uint32_t w[8];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) x[i] = u2f(u[h][i]);
-                        if (need_mask) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (kb + i > hi || kb + i < lo) x[i] = -INFINITY;
-                        }
-                        uint32_t w[8];
+                    for (int k = 0; k < 8; ++k) {
+                        float x0, x1, x2, x3;
+                        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k]), u2f(u[g][4 * k + 1])), c2, b2), x0, x1);
+                        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k + 2]), u2f(u[g][4 * k + 3])), c2, b2), x2, x3);
+                        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
+                        acc0 = ptx::fadd2(acc0, ptx::f2pack(p0, p1));
+                        acc1 = ptx::fadd2(acc1, ptx::f2pack(p2, p3));
+                        w[k] = ptx::cvt_e4m3x2(p1, p0) | (ptx::cvt_e4m3x2(p3, p2) << 16);
+                        u[g][4 * k] = __float_as_uint(p0);
+                        u[g][4 * k + 1] = __float_as_uint(p1);
+                        u[g][4 * k + 2] = __float_as_uint(p2);
+                        u[g][4 * k + 3] = __float_as_uint(p3);
+                    }
+                    ptx::tmem_st8(scol + 32 * g, w);
+                    if (need_mask) {
+                        // second E4M3 term on masked tiles: P_lo = e4m3(p - P_hi)
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
-                            float x0, x1, x2, x3;
-                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(x[4 * k], x[4 * k + 1]), c2, b2), x0, x1);
-                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(x[4 * k + 2], x[4 * k + 3]), c2, b2), x2, x3);
-                            x[4 * k] = ptx::ex2(x0);
-                            x[4 * k + 1] = ptx::ex2(x1);
-                            x[4 * k + 2] = ptx::ex2(x2);
-                            x[4 * k + 3] = ptx::ex2(x3);
-                            acc0 = ptx::fadd2(acc0, ptx::f2pack(x[4 * k], x[4 * k + 1]));
-                            acc1 = ptx::fadd2(acc1, ptx::f2pack(x[4 * k + 2], x[4 * k + 3]));
-                            w[k] = ptx::cvt_e4m3x2(x[4 * k + 1], x[4 * k]) |
-                                   (ptx::cvt_e4m3x2(x[4 * k + 3], x[4 * k + 2]) << 16);
+                            float q0, q1, q2, q3;
+                            ptx::e4m3x2_to_f32(w[k] & 0xFFFFu, q0, q1);
+                            ptx::e4m3x2_to_f32(w[k] >> 16, q2, q3);
+                            w[k] = ptx::cvt_e4m3x2(u2f(u[g][4 * k + 1]) - q1, u2f(u[g][4 * k]) - q0) |
+                                   (ptx::cvt_e4m3x2(u2f(u[g][4 * k + 3]) - q3, u2f(u[g][4 * k + 2]) - q2) << 16);
                         }
-                        ptx::tmem_st8(scol + kb, w);
-                        if (need_mask) {
-                            // second E4M3 term on masked tiles: P_lo = e4m3(p - P_hi)
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                float q0, q1, q2, q3;
-                                ptx::e4m3x2_to_f32(w[k] & 0xFFFFu, q0, q1);
-                                ptx::e4m3x2_to_f32(w[k] >> 16, q2, q3);
-                                w[k] = ptx::cvt_e4m3x2(x[4 * k + 1] - q1, x[4 * k] - q0) |
-                                       (ptx::cvt_e4m3x2(x[4 * k + 3] - q3, x[4 * k + 2] - q2) << 16);
-                            }
-                            ptx::tmem_st8(scol + kb + 8, w);
-                        }
+                        ptx::tmem_st8(scol + 32 * g + 8, w);
                     }
                 }
                 ptx::tmem_wait_st();
@@ -726,35 +713,49 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::tc_fence_before();
             ptx::mbar_arrive(BAR(C::B_PF + sb));
             if (tid == 0) FA8_EV(5, it);
-            if (!W.wait_warp(BAR(C::B_AE + (it & 1)), ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
-            alpha_ring[(it & 1) * 128 + r] = alpha;
-            ptx::mbar_arrive(BAR(C::B_AF + (it & 1)));
-            if (tid == 0) FA8_EV(6, it);
+            if (h == 0) {
+                if (!W.wait_warp(BAR(C::B_AE + (it & 1)), ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
+                alpha_ring[(it & 1) * 128 + r] = alpha;
+                ptx::mbar_arrive(BAR(C::B_AF + (it & 1)));
+                if (tid == 0) FA8_EV(6, it);
+            }
         }
-        // finalize: the 2^8 bias cancels between O and row_sum and is removed from the LSE
-        float scale_o = 0.f, lse;
-        const float sig = has_sink ? p.sink[hq] : 0.f;
-        if (m_run == -INFINITY) {
-            lse = has_sink ? sig : -INFINITY;
+        // combine the two halves' row sums, then finalize: the 2^8 bias cancels between O
+        // and row_sum and is removed from the LSE
+        if (h == 1) {
+            sum_part[r] = row_sum;
+            ptx::mbar_arrive(BAR(C::B_SUM));
         } else {
-            const float sl2 = sig * kLog2e;
-            const float m_f = (has_sink && sl2 > m_run) ? sl2 : m_run;
-            const float sc = ptx::ex2(m_run - m_f);
-            const float rs = row_sum * sc + (has_sink ? ptx::ex2(sl2 - m_f + kPBias) : 0.f);
-            scale_o = sc * dvv / rs;
-            lse = (ptx::lg2(rs) + m_f - kPBias) * kLn2;
+            const bool got = W.wait_warp(BAR(C::B_SUM), 0);
+            row_sum += got ? sum_part[r] : 0.f;
+            const float dvv = p.dv ? p.dv[b * p.dv_sb + kvh * p.dv_sh] : 1.f;
+            float scale_o = 0.f, lse;
+            const float sig = has_sink ? p.sink[hq] : 0.f;
+            if (m_run == -INFINITY) {
+                lse = has_sink ? sig : -INFINITY;
+            } else {
+                const float sl2 = sig * kLog2e;
+                const float m_f = (has_sink && sl2 > m_run) ? sl2 : m_run;
+                const float sc = ptx::ex2(m_run - m_f);
+                const float rs = row_sum * sc + (has_sink ? ptx::ex2(sl2 - m_f + kPBias) : 0.f);
+                scale_o = sc * dvv / rs;
+                lse = (ptx::lg2(rs) + m_f - kPBias) * kLn2;
+            }
+            row_scale[r] = scale_o;
+            ptx::mbar_arrive(BAR(C::B_FIN));
+            if (row_ok) {
+                if (p.split_mode)
+                    p.lse_part[((long long)split * p.total_q + tok) * p.Hq + hq] = lse;
+                else if (p.lse)
+                    p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
+            }
         }
-        row_scale[r] = scale_o;
-        if (row_ok) {
-            if (p.split_mode)
-                p.lse_part[((long long)split * p.total_q + tok) * p.Hq + hq] = lse;
-            else if (p.lse)
-                p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
-        }
-        ptx::named_bar_sync(1, 256);
-      } else {
-        // ======================================================== correction (warps 4-7)
-        const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+      }
+    } else {
+      ptx::setmaxnreg_inc<kRegsCorr>();
+      {
+        // ======================================================== correction (warps 8-11)
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const bool warp_active = __any_sync(0xffffffffu, row_ok);
         float o[C::O_REGS ? DV : 1];
 #pragma unroll
@@ -823,8 +824,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 ++pv_uses;
             }
         }
-        ptx::named_bar_sync(1, 256);
-        const float sc = row_scale[r];
+        const bool fin = W.wait_warp(BAR(C::B_FIN), 0);
+        const float sc = fin ? row_scale[r] : 0.f;
         // TMEM loads are warp-collective (.sync.aligned): the whole active warp loads, only
         // the valid rows store.
         if (warp_active) {
@@ -890,7 +891,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     if (tid == 0) FA8_EV(15, 1);
-    if (warp == 9) {
+    if (warp == 13) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::TM_COLS);
     }

@@ -6,18 +6,12 @@
 #include <cuda_runtime.h>
 
 #include "fa8_kernel.cuh"
-#include "fa8_kernel2.cuh"
 
 namespace fa8 {
 
 template <int D, int DV>
 cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                        const CUtensorMap &tv, dim3 grid, cudaStream_t stream);
-
-// two-Q-tile (prefill) form, dv <= 128
-template <int D, int DV>
-cudaError_t launch_fwd2(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                        const CUtensorMap &tv, dim3 grid, cudaStream_t stream);
 
 template <int DV>
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
@@ -36,20 +30,6 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
                                              smem);                                          \
         if (e != cudaSuccess) return e;                                                      \
         fwd_kernel<D_, DV_><<<grid, kNumThreads, smem, stream>>>(p, tq, tk, tv);             \
-        return cudaGetLastError();                                                           \
-    }
-
-#define FA8_DEFINE_FWD2(D_, DV_)                                                             \
-    template <>                                                                              \
-    cudaError_t launch_fwd2<D_, DV_>(const FwdParams &p, const CUtensorMap &tq,              \
-                                     const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid, \
-                                     cudaStream_t stream) {                                  \
-        constexpr int smem = Cfg2<D_, DV_>::SMEM_BYTES;                                      \
-        cudaError_t e = cudaFuncSetAttribute(fwd2_kernel<D_, DV_>,                           \
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,    \
-                                             smem);                                          \
-        if (e != cudaSuccess) return e;                                                      \
-        fwd2_kernel<D_, DV_><<<grid, kNumThreads, smem, stream>>>(p, tq, tk, tv);            \
         return cudaGetLastError();                                                           \
     }
 
