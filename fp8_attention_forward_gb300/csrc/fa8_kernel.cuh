@@ -153,9 +153,10 @@ struct Cfg {
     static constexpr int B_PF = B_SF + NS;
     static constexpr int B_OF = B_PF + NS;   // NOT slots
     static constexpr int B_OE = B_OF + NOT;  // NOT slots
-    static constexpr int B_AF = B_OE + NOT;  // 2 slots
-    static constexpr int B_AE = B_AF + 2;  // 2 slots
-    static constexpr int B_XCH = B_AE + 2;   // 2 slots: row-max exchange between the halves
+    static constexpr int NA = 4;             // alpha ring depth (softmax -> correction)
+    static constexpr int B_AF = B_OE + NOT;  // NA slots
+    static constexpr int B_AE = B_AF + NA;   // NA slots
+    static constexpr int B_XCH = B_AE + NA;  // 2 slots: row-max exchange between the halves
     static constexpr int B_SUM = B_XCH + 2;  // half 1 -> half 0: final partial row sums
     static constexpr int B_FIN = B_SUM + 1;  // half 0 -> correction: final O scale
     static constexpr int B_DONE = B_FIN + 1;
@@ -393,10 +394,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc + 512);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 516);
-    float *alpha_ring = reinterpret_cast<float *>(misc + 1024);  // [2][128]
-    float *row_scale = reinterpret_cast<float *>(misc + 2048);   // [128]
-    float *mx_part = reinterpret_cast<float *>(misc + 2560);     // [2 parity][2 half][128]
-    float *sum_part = reinterpret_cast<float *>(misc + 4608);    // [128]
+    float *alpha_ring = reinterpret_cast<float *>(misc + 1024);  // [NA][128]
+    float *row_scale = reinterpret_cast<float *>(misc + 3072);   // [128]
+    float *mx_part = reinterpret_cast<float *>(misc + 3584);     // [2 parity][2 half][128]
+    float *sum_part = reinterpret_cast<float *>(misc + 5632);    // [128]
     const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
     const uint32_t sK = ptx::smem_u32(smem + C::OFF_K);
     const uint32_t sV = ptx::smem_u32(smem + C::OFF_V);
@@ -417,11 +418,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_init(BAR(C::B_OF + i), 1);
             ptx::mbar_init(BAR(C::B_OE + i), 128);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NA; ++i) {
             ptx::mbar_init(BAR(C::B_AF + i), 128);
             ptx::mbar_init(BAR(C::B_AE + i), 128);
-            ptx::mbar_init(BAR(C::B_XCH + i), 256);
         }
+        for (int i = 0; i < 2; ++i) ptx::mbar_init(BAR(C::B_XCH + i), 256);
         ptx::mbar_init(BAR(C::B_SUM), 128);
         ptx::mbar_init(BAR(C::B_FIN), 128);
         ptx::mbar_init(BAR(C::B_DONE), 1);
@@ -480,7 +481,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int c3 = p.kv_mode == 1 ? 0 : b;
             // K tile
             if (!W.wait_warp(BAR(C::B_KE + st), ph ^ 1u)) break;
-            if (lane == 0) FA8_EV(0, it);
             if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_KF + st), (uint32_t)C::K_BYTES);
             __syncwarp();
             const uint32_t dK = sK + st * C::K_BYTES;
@@ -499,7 +499,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             issued_k = it + 1;
             // V tile
             if (!W.wait_warp(BAR(C::B_VE + st), ph ^ 1u)) break;
-            if (lane == 0) FA8_EV(1, it);
             if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_VF + st), (uint32_t)C::V_BYTES);
             __syncwarp();
             const uint32_t dV = sV + st * C::V_BYTES;
@@ -529,83 +528,86 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         __syncwarp();
     } else if (warp == 13) {
         // ======================================================== MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t kIdescQK = idesc_e4m3(kTileM, kTileN, false);
-            constexpr uint32_t kIdescPV = idesc_e4m3(kTileM, C::OTW, true);
-            int pv_uses = 0;
-            bool ok = W.wait(BAR(C::B_Q), 0);
+        // The whole warp runs this loop (uniform control flow); one elected lane issues the
+        // tcgen05 operations.  Shared-memory descriptors are built once and advanced by
+        // compile-time byte offsets (start-address field, units of 16 bytes).
+        constexpr uint32_t kIdescQK = idesc_e4m3(kTileM, kTileN, false);
+        constexpr uint32_t kIdescPV = idesc_e4m3(kTileM, C::OTW, true);
+        const uint64_t dq0 = sdesc(sQ, 16, 8 * C::CW, swz_layout(C::CW));
+        const uint64_t dk0 = sdesc(sK, 16, 8 * C::CW, swz_layout(C::CW));
+        const uint64_t dv0 = sdesc(sV, C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
+        const bool leader = ptx::elect_one();
+        int pv_uses = 0;
+        bool ok = W.wait_warp(BAR(C::B_Q), 0);
+        ptx::tc_fence_after();
+        auto do_pv = [&](int j) -> bool {
+            const int sb = j % C::NS;
+            const int vs = j % C::STAGES;
+            if (!W.wait_warp(BAR(C::B_PF + sb), (uint32_t)(j / C::NS) & 1u)) return false;
+            FA8_EV(10, j);
+            if (!W.wait_warp(BAR(C::B_VF + vs), (uint32_t)(j / C::STAGES) & 1u)) return false;
+            FA8_EV(11, j);
             ptx::tc_fence_after();
-            auto do_pv = [&](int j) -> bool {
-                const int sb = j % C::NS;
-                const int vs = j % C::STAGES;
-                FA8_EV(13, j);
-                if (!W.wait(BAR(C::B_PF + sb), (uint32_t)(j / C::NS) & 1u)) return false;
-                FA8_EV(10, j);
-                if (!W.wait(BAR(C::B_VF + vs), (uint32_t)(j / C::STAGES) & 1u)) return false;
-                FA8_EV(11, j);
-                ptx::tc_fence_after();
-                const uint32_t vbase = sV + vs * C::V_BYTES;
-                const bool two_term = tile_needs_mask((t_beg + j) * kTileN, Lk, p.causal, p.window_left, pos0,
-                                                      pos_last, delta);
+            const bool two_term = tile_needs_mask((t_beg + j) * kTileN, Lk, p.causal, p.window_left, pos0,
+                                                  pos_last, delta);
+            const uint64_t dv_stage = dv0 + (uint64_t)((vs * C::V_BYTES) >> 4);
+            const uint32_t s_col = tmem + C::TM_S + sb * 128;
 #pragma unroll
-                for (int c = 0; c < C::NPV; ++c) {
-                    const int ob = pv_uses % C::NOT;
-                    const uint32_t otile = tmem + C::TM_OT + ob * C::OTW;
-                    if (!W.wait(BAR(C::B_OE + ob), ((uint32_t)(pv_uses / C::NOT) & 1u) ^ 1u)) return false;
-                    FA8_EV(12, j);
-                    ptx::tc_fence_after();
+            for (int c = 0; c < C::NPV; ++c) {
+                const int ob = pv_uses % C::NOT;
+                const uint32_t otile = tmem + C::TM_OT + ob * C::OTW;
+                if (!W.wait_warp(BAR(C::B_OE + ob), ((uint32_t)(pv_uses / C::NOT) & 1u) ^ 1u)) return false;
+                FA8_EV(12, j);
+                ptx::tc_fence_after();
+                if (leader) {
 #pragma unroll
                     for (int kk = 0; kk < kTileN / 32; ++kk) {
-                        const uint32_t a = tmem + C::TM_S + sb * 128 + kk * 32;
-                        const uint64_t bd =
-                            sdesc(vbase + (c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV,
-                                  C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
-                        ptx::mma_f8_ts(otile, a, bd, kIdescPV, kk > 0 ? 1u : 0u);
+                        const uint64_t bd = dv_stage + (uint64_t)(((c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV) >> 4);
+                        ptx::mma_f8_ts(otile, s_col + kk * 32, bd, kIdescPV, kk > 0 ? 1u : 0u);
                     }
                     if (two_term) {  // + P_lo V (P_lo 8 columns after each P_hi slice)
 #pragma unroll
                         for (int kk = 0; kk < kTileN / 32; ++kk) {
-                            const uint32_t a = tmem + C::TM_S + sb * 128 + kk * 32 + 8;
-                            const uint64_t bd =
-                                sdesc(vbase + (c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV,
-                                      C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
-                            ptx::mma_f8_ts(otile, a, bd, kIdescPV, 1u);
+                            const uint64_t bd = dv_stage + (uint64_t)(((c * C::OTW / C::CWV) * C::CHUNK_V + kk * 32 * C::CWV) >> 4);
+                            ptx::mma_f8_ts(otile, s_col + kk * 32 + 8, bd, kIdescPV, 1u);
                         }
                     }
                     ptx::tc_commit(BAR(C::B_OF + ob));
-                    ++pv_uses;
                 }
-                ptx::tc_commit(BAR(C::B_VE + vs));
-                FA8_EV(3, j);
-                return true;
-            };
-            for (int it = 0; ok && it < n_tiles; ++it) {
-                const int ks = it % C::STAGES;
-                if (!W.wait(BAR(C::B_KF + ks), (uint32_t)(it / C::STAGES) & 1u)) { ok = false; break; }
-                FA8_EV(9, it);
-                ptx::tc_fence_after();
-                if (C::NS == 1 && it > 0 && !do_pv(it - 1)) { ok = false; break; }
-                const int sb = it % C::NS;
-                const uint32_t kbase = sK + ks * C::K_BYTES;
+                __syncwarp();
+                ++pv_uses;
+            }
+            if (leader) ptx::tc_commit(BAR(C::B_VE + vs));
+            __syncwarp();
+            FA8_EV(3, j);
+            return true;
+        };
+        for (int it = 0; ok && it < n_tiles; ++it) {
+            const int ks = it % C::STAGES;
+            if (!W.wait_warp(BAR(C::B_KF + ks), (uint32_t)(it / C::STAGES) & 1u)) { ok = false; break; }
+            FA8_EV(9, it);
+            ptx::tc_fence_after();
+            if (C::NS == 1 && it > 0 && !do_pv(it - 1)) { ok = false; break; }
+            const int sb = it % C::NS;
+            const uint64_t dk_stage = dk0 + (uint64_t)((ks * C::K_BYTES) >> 4);
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < D / 32; ++kk) {
-                    const int chunk = (kk * 32) / C::CW;
-                    const int off = (kk * 32) % C::CW;
-                    const uint64_t qd = sdesc(sQ + chunk * C::CHUNK_Q + off, 16, 8 * C::CW, swz_layout(C::CW));
-                    const uint64_t kd = sdesc(kbase + chunk * C::CHUNK_K + off, 16, 8 * C::CW, swz_layout(C::CW));
-                    ptx::mma_f8_ss(tmem + C::TM_S + sb * 128, qd, kd, kIdescQK, kk > 0 ? 1u : 0u);
+                    const uint32_t off = (uint32_t)((((kk * 32) / C::CW) * C::CHUNK_Q + (kk * 32) % C::CW) >> 4);
+                    ptx::mma_f8_ss(tmem + C::TM_S + sb * 128, dq0 + off, dk_stage + off, kIdescQK, kk > 0 ? 1u : 0u);
                 }
-                FA8_EV(14, it);
                 ptx::tc_commit(BAR(C::B_SF + sb));
                 ptx::tc_commit(BAR(C::B_KE + ks));
-                FA8_EV(2, it);
-                if (C::NS == 2 && it > 0 && !do_pv(it - 1)) { ok = false; break; }
             }
-            if (ok) ok = do_pv(n_tiles - 1);
-            // all MMAs must finish before TMEM is released
-            ptx::tc_commit(BAR(C::B_DONE));
-            W.drain(BAR(C::B_DONE), 0);
+            __syncwarp();
+            FA8_EV(2, it);
+            if (C::NS == 2 && it > 0 && !do_pv(it - 1)) { ok = false; break; }
         }
+        if (ok) ok = do_pv(n_tiles - 1);
+        // all MMAs must finish before TMEM is released
+        if (leader) ptx::tc_commit(BAR(C::B_DONE));
+        __syncwarp();
+        W.drain(BAR(C::B_DONE), 0);
         __syncwarp();
       }
     } else if (warp < 8) {
@@ -639,6 +641,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 ptx::tmem_wait_ld();
                 ptx::reg_fence32(u[0]);
                 ptx::reg_fence32(u[1]);
+                if (tid == 0) FA8_EV(0, it);
                 if (need_mask) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
@@ -660,6 +663,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_arrive(BAR(C::B_XCH + (it & 1)));
             if (!W.wait_warp(BAR(C::B_XCH + (it & 1)), (uint32_t)(it >> 1) & 1u)) break;
             const float mx = fmaxf(mh, mx_part[((it & 1) * 2 + (h ^ 1)) * 128 + r]);
+            if (tid == 0) FA8_EV(1, it);
             float alpha = 1.f;
             if (warp_active) {
                 const float mt = mx * c;
@@ -704,6 +708,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         ptx::tmem_st8(scol + 32 * g + 8, w);
                     }
                 }
+                if (tid == 0) FA8_EV(13, it);
                 ptx::tmem_wait_st();
                 float a0, a1, a2, a3;
                 ptx::f2unpack(acc0, a0, a1);
@@ -714,9 +719,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_arrive(BAR(C::B_PF + sb));
             if (tid == 0) FA8_EV(5, it);
             if (h == 0) {
-                if (!W.wait_warp(BAR(C::B_AE + (it & 1)), ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
-                alpha_ring[(it & 1) * 128 + r] = alpha;
-                ptx::mbar_arrive(BAR(C::B_AF + (it & 1)));
+                const int as = it % C::NA;
+                if (!W.wait_warp(BAR(C::B_AE + as), ((uint32_t)(it / C::NA) & 1u) ^ 1u)) break;
+                alpha_ring[as * 128 + r] = alpha;
+                ptx::mbar_arrive(BAR(C::B_AF + as));
                 if (tid == 0) FA8_EV(6, it);
             }
         }
@@ -763,14 +769,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         int pv_uses = 0;
         bool ok = true;
         for (int it = 0; ok && it < n_tiles; ++it) {
-            if (!W.wait_warp(BAR(C::B_AF + (it & 1)), (uint32_t)(it >> 1) & 1u)) break;
-            const float alpha = alpha_ring[(it & 1) * 128 + r];
-            ptx::mbar_arrive(BAR(C::B_AE + (it & 1)));
+            const int as = it % C::NA;
+            if (!W.wait_warp(BAR(C::B_AF + as), (uint32_t)(it / C::NA) & 1u)) break;
+            const float alpha = alpha_ring[as * 128 + r];
+            ptx::mbar_arrive(BAR(C::B_AE + as));
 #pragma unroll
             for (int c = 0; c < C::NPV; ++c) {
                 const int ob = pv_uses % C::NOT;
                 if (!W.wait_warp(BAR(C::B_OF + ob), (uint32_t)(pv_uses / C::NOT) & 1u)) { ok = false; break; }
-                if (tid == 128 && c == 0) FA8_EV(7, it);
+                if (tid == 256 && c == 0) FA8_EV(7, it);
                 ptx::tc_fence_after();
                 const uint32_t otile = tmem + lane_base + C::TM_OT + ob * C::OTW;
                 if (warp_active) {
@@ -820,7 +827,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(BAR(C::B_OE + ob));
-                if (tid == 128 && c == C::NPV - 1) FA8_EV(8, it);
+                if (tid == 256 && c == C::NPV - 1) FA8_EV(8, it);
                 ++pv_uses;
             }
         }
