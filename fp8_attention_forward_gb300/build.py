@@ -52,16 +52,17 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None,
-          out_dir: str | None = None, defines=()) -> str:
+          out_dir: str | None = None, defines=(), src_dir: str | None = None) -> str:
     """Compiles csrc/*.cu and links libfa8.so into ``out_dir`` (default: the in-tree
-    _build/); ``defines`` are extra -D macros (e.g. FA8_TRACE for the pipeline trace)."""
+    _build/); ``defines`` are extra -D macros (e.g. FA8_TRACE for the pipeline trace);
+    ``src_dir`` compiles another copy of the sources instead of csrc/."""
     build_dir = out_dir or BUILD
     lib = os.path.join(build_dir, "libfa8.so")
-    if not force and not ptxas_verbose and not defines and out_dir is None and up_to_date():
+    if not force and not ptxas_verbose and not defines and out_dir is None and src_dir is None and up_to_date():
         return LIB
     os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    srcs = _sources()
+    srcs = sorted(glob.glob(os.path.join(src_dir, "*.cu"))) if src_dir else _sources()
     objs = [os.path.join(build_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
 
     def one(pair):

@@ -13,7 +13,7 @@
 #include <numeric>
 #include <string>
 
-#include "../../include/fa8.h"
+#include "fa8.h"
 #include "fa8_launch.h"
 
 // Device status word of the library (timeouts, out-of-range block-table entries),

@@ -3,17 +3,16 @@
 //
 // One CTA computes one 128-row Q tile: the rows are (query position, q-head) pairs of one
 // kv-head group, packed position-major (PackGQA), against the kv-head's keys, for one
-// split of the request's key range.  Roles (512 threads, four warpgroups):
-//   warps 0-3   softmax, keys [0, 64) of every tile: thread r owns TMEM lane r = row r
-//   warps 4-7   softmax, keys [64, 128) of the same rows; the two halves exchange their
-//               row maxima once per tile and their row sums once at the end
-//   warps 8-11  correction: two-level PV fold into fp32 O, epilogue
-//   warp 12     TMA producer (Q once, K/V tiles into S-stage rings)
-//   warp 13     MMA issuer (lane 0) and TMEM owner
-//   warps 14-15 idle (the control warpgroup gives its registers to the correction)
-// Splitting each row over two warps halves the per-warp softmax work per tile, so the
-// softmax keeps pace with the tensor core; each half reads its 64 S columns from TMEM in a
-// single round trip per tile.
+// split of the request's key range.  Roles (384 threads, three warpgroups):
+//   warps 0-3   half 0 of every row: keys [0, 64) of each tile and O columns [0, dv/2)
+//   warps 4-7   half 1 of the same rows: keys [64, 128) and O columns [dv/2, dv)
+//               (thread r of a half owns TMEM lane r = tile row r)
+//   warp 8      TMA producer (Q once, K/V tiles into S-stage rings)
+//   warp 9      MMA issuer (one elected lane) and TMEM owner
+//   warps 10-11 idle (the control warpgroup gives its registers to the two halves)
+// Each half does the softmax of its 64 keys and the two-level fold of its half of O; the
+// two halves exchange their row maxima once per tile (so both use the same running max
+// and rescale factor) and their row sums once at the end.
 //
 // Per 128-key tile t (sources: "[Cute,Fwd,Sm90] Native FP8 (E4M3 Q/K/V) forward for
 // Hopper", Design; "tml-fa4 PR #4", Summary and "Correctness fix over #1"):
@@ -42,10 +41,9 @@ namespace fa8 {
 
 constexpr int kTileM = 128;     // Q rows per CTA = TMEM lanes
 constexpr int kTileN = 128;     // keys per KV tile
-constexpr int kNumThreads = 512;
-// registers per thread after setmaxnreg; 256 x 112 + 128 x 240 + 128 x 48 = 512 x 128 (launch)
-constexpr int kRegsSoft = 112;
-constexpr int kRegsCorr = 240;
+constexpr int kNumThreads = 384;
+// registers per thread after setmaxnreg; 256 x 224 + 128 x 48 <= 384 x 168 (launch)
+constexpr int kRegsMath = 224;
 constexpr int kRegsCtl = 48;
 constexpr float kTau = 0.75f;   // lazy-rescale threshold, log2 units
 constexpr float kPBias = 8.0f;  // P carries a factor 2^8
@@ -55,15 +53,19 @@ constexpr float kLn2 = 0.6931471805599453f;
 enum : unsigned { kStatusTimeout = 1u, kStatusBounds = 2u };
 
 // Pipeline event trace (compiled in only with -DFA8_TRACE): clock64() per (CTA, event, tile)
-// for the first kTraceCtas CTAs of grid row 0; layout [cta][event][tile].
+// for the first kTraceCtas CTAs of grid row 0; layout [cta][event][tile].  Events are kept
+// in shared memory while the CTA runs (a global store before an mbarrier arrive would
+// delay the arrive's release) and copied out at the end.
 constexpr int kTraceCtas = 8, kTraceEvents = 16, kTraceTiles = 64;
 #ifdef FA8_TRACE
-#define FA8_EV(ev, it)                                                                            \
-    do {                                                                                          \
-        if (p.trace && blockIdx.y == 0 && blockIdx.x < kTraceCtas && (it) < kTraceTiles)          \
-            p.trace[((size_t)blockIdx.x * kTraceEvents + (ev)) * kTraceTiles + (it)] = clock64(); \
+constexpr int kTraceSmemBytes = kTraceEvents * kTraceTiles * 8;
+#define FA8_EV(ev, it)                                                                  \
+    do {                                                                                \
+        if ((it) < kTraceTiles)                                                         \
+            reinterpret_cast<unsigned long long *>(smem + C::OFF_TRACE)[(ev) * kTraceTiles + (it)] = clock64(); \
     } while (0)
 #else
+constexpr int kTraceSmemBytes = 0;
 #define FA8_EV(ev, it) \
     do {               \
     } while (0)
@@ -136,13 +138,15 @@ struct Cfg {
     static constexpr int V_BYTES = kTileN * DV;
     static constexpr int MISC_BYTES = 6144;
     static constexpr int SMEM_LIMIT = 232448;  // max dynamic smem per block on sm_103
-    static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - MISC_BYTES - Q_BYTES) / (K_BYTES + V_BYTES);
+    static constexpr int STAGES_FIT =
+        (SMEM_LIMIT - 1024 - MISC_BYTES - kTraceSmemBytes - Q_BYTES) / (K_BYTES + V_BYTES);
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = Q_BYTES;
     static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
     static constexpr int OFF_MISC = OFF_V + STAGES * V_BYTES;
-    static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
+    static constexpr int OFF_TRACE = OFF_MISC + MISC_BYTES;
+    static constexpr int SMEM_BYTES = OFF_TRACE + kTraceSmemBytes + 1024;
     // barrier slots
     static constexpr int B_Q = 0;
     static constexpr int B_KF = 1;
@@ -153,19 +157,16 @@ struct Cfg {
     static constexpr int B_PF = B_SF + NS;
     static constexpr int B_OF = B_PF + NS;   // NOT slots
     static constexpr int B_OE = B_OF + NOT;  // NOT slots
-    static constexpr int NA = 4;             // alpha ring depth (softmax -> correction)
-    static constexpr int B_AF = B_OE + NOT;  // NA slots
-    static constexpr int B_AE = B_AF + NA;   // NA slots
-    static constexpr int B_XCH = B_AE + NA;  // 2 slots: row-max exchange between the halves
-    static constexpr int B_SUM = B_XCH + 2;  // half 1 -> half 0: final partial row sums
-    static constexpr int B_FIN = B_SUM + 1;  // half 0 -> correction: final O scale
-    static constexpr int B_DONE = B_FIN + 1;
+    static constexpr int B_XCH = B_OE + NOT;  // 2 slots: row-max exchange between the halves
+    static constexpr int B_SUM = B_XCH + 2;   // final partial row sums of both halves
+    static constexpr int B_DONE = B_SUM + 1;
     static constexpr int NUM_BARS = B_DONE + 1;
     static_assert(STAGES >= 2, "smem too small for two K/V stages");
     static_assert(NUM_BARS * 8 <= 512, "barrier area");
     static_assert(TM_OR + (O_REGS ? 0 : DV) <= TM_COLS, "TMEM budget");
     static_assert(OTW % CWV == 0 && OTW % 32 == 0 && OTW % 16 == 0 && OTW <= 256, "PV shape");
     static_assert(D % 32 == 0 && DV % 32 == 0, "head dims");
+    static_assert(OTW % 64 == 0, "each half folds a multiple of 32 columns of every O_tile chunk");
 };
 
 // UMMA shared-memory descriptor: start >>4 [0,14), LBO >>4 [16,30), SBO >>4 [32,46),
@@ -193,12 +194,11 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn_major)
 // Bounded mbarrier waits: give up when another role aborted or after timeout_ns, setting
 // the CTA abort flag and the device status word.
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
-                                       unsigned long long timeout, unsigned int *status) {
+                                          unsigned long long timeout, unsigned int *status) {
     const uint64_t t0 = ptx::globaltimer();
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (ptx::mbar_try_wait(bar, parity)) return true;
+        // sleeps in hardware (up to 20 us per try) instead of spinning on issue slots
+        if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort) return false;
         if (ptx::globaltimer() - t0 > timeout) {
             *abort = 1;
@@ -281,6 +281,13 @@ __device__ __forceinline__ bool varlen_slot(const FwdParams &p, int x, int &b, i
 }
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// O column of the j-th 32-column slice owned by half h: half h folds columns
+// [c*OTW + h*OTW/2, c*OTW + (h+1)*OTW/2) of every O_tile chunk c.
+template <class C>
+__host__ __device__ constexpr int out_col(int h, int j) {
+    return (j / (C::OTW / 64)) * C::OTW + (C::OTW / 2) * h + (j % (C::OTW / 64)) * 32;
+}
 
 // Writes 8 consecutive output values (one 16-byte store) in bf16 or fp16.
 __device__ __forceinline__ void store8(void *dst, const float *v, int fp16) {
@@ -394,10 +401,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc + 512);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 516);
-    float *alpha_ring = reinterpret_cast<float *>(misc + 1024);  // [NA][128]
-    float *row_scale = reinterpret_cast<float *>(misc + 3072);   // [128]
-    float *mx_part = reinterpret_cast<float *>(misc + 3584);     // [2 parity][2 half][128]
-    float *sum_part = reinterpret_cast<float *>(misc + 5632);    // [128]
+    float *mx_part = reinterpret_cast<float *>(misc + 1024);   // [2 parity][2 half][128]
+    float *sum_part = reinterpret_cast<float *>(misc + 3072);  // [2 half][128]
     const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
     const uint32_t sK = ptx::smem_u32(smem + C::OFF_K);
     const uint32_t sV = ptx::smem_u32(smem + C::OFF_V);
@@ -416,26 +421,25 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         for (int i = 0; i < C::NOT; ++i) {
             ptx::mbar_init(BAR(C::B_OF + i), 1);
-            ptx::mbar_init(BAR(C::B_OE + i), 128);
-        }
-        for (int i = 0; i < C::NA; ++i) {
-            ptx::mbar_init(BAR(C::B_AF + i), 128);
-            ptx::mbar_init(BAR(C::B_AE + i), 128);
+            ptx::mbar_init(BAR(C::B_OE + i), 256);
         }
         for (int i = 0; i < 2; ++i) ptx::mbar_init(BAR(C::B_XCH + i), 256);
-        ptx::mbar_init(BAR(C::B_SUM), 128);
-        ptx::mbar_init(BAR(C::B_FIN), 128);
+        ptx::mbar_init(BAR(C::B_SUM), 256);
         ptx::mbar_init(BAR(C::B_DONE), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
     }
-    if (warp == 12 && lane == 0) {
+#ifdef FA8_TRACE
+    for (int i = tid; i < kTraceEvents * kTraceTiles; i += kNumThreads)
+        reinterpret_cast<unsigned long long *>(smem + C::OFF_TRACE)[i] = 0ull;
+#endif
+    if (warp == 8 && lane == 0) {
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
     }
-    if (warp == 13) {
+    if (warp == 9) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TM_COLS);
         ptx::tmem_relinquish();
     }
@@ -446,9 +450,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const Waiter W{abort_flag, p.timeout_ns, p.status};
     if (tid == 0) FA8_EV(15, 0);
 
-    if (warp >= 12) {
+    if (warp >= 8) {
       ptx::setmaxnreg_dec<kRegsCtl>();
-      if (warp == 12) {
+      if (warp == 8) {
         // ======================================================== TMA producer
         const bool paged = p.kv_mode == 2;
         int issued_k = 0, issued_v = 0;
@@ -526,7 +530,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 W.drain(BAR(C::B_VF + i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u);
         }
         __syncwarp();
-    } else if (warp == 13) {
+    } else if (warp == 9) {
         // ======================================================== MMA issuer
         // The whole warp runs this loop (uniform control flow); one elected lane issues the
         // tcgen05 operations.  Shared-memory descriptors are built once and advanced by
@@ -610,11 +614,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         W.drain(BAR(C::B_DONE), 0);
         __syncwarp();
       }
-    } else if (warp < 8) {
-      ptx::setmaxnreg_dec<kRegsSoft>();
+    } else {
+      ptx::setmaxnreg_inc<kRegsMath>();
       {
-        // ======================================================== softmax (half h of each row)
-        const int h = warp >> 2;  // keys [64 h, 64 h + 64) of every tile
+        // ======================================================== softmax + fold (half h)
+        constexpr int HDV = DV / 2;   // O columns of this half
+        constexpr int HOT = C::OTW / 2;  // columns of each O_tile chunk folded by this half
+        const int h = warp >> 2;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const bool warp_active = __any_sync(0xffffffffu, row_ok);
         const float dqv = p.dq ? p.dq[b * p.dq_sb + kvh * p.dq_sh] : 1.f;
@@ -623,239 +629,217 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const uint64_t c2 = ptx::f2pack(c, c);
         const int hi_row = p.causal ? min(Lk - 1, rpos + delta) : Lk - 1;
         const int lo_row = p.window_left >= 0 ? max(0, rpos + delta - p.window_left) : 0;
+        float o[C::O_REGS ? HDV : 1];
+#pragma unroll
+        for (int i = 0; i < (C::O_REGS ? HDV : 1); ++i) o[i] = 0.f;
         float m_run = -INFINITY, row_sum = 0.f;  // identical m_run in both halves
-        for (int it = 0; it < n_tiles; ++it) {
-            const int k0 = (t_beg + it) * kTileN;
-            const int sb = it % C::NS;
-            if (!W.wait_warp(BAR(C::B_SF + sb), (uint32_t)(it / C::NS) & 1u)) break;
-            if (tid == 0) FA8_EV(4, it);
-            ptx::tc_fence_after();
-            const uint32_t scol = tmem + lane_base + C::TM_S + sb * 128 + 64 * h;
-            const bool need_mask = tile_needs_mask(k0, Lk, p.causal, p.window_left, pos0, pos_last, delta);
-            const int hi = hi_row - k0 - 64 * h, lo = lo_row - k0 - 64 * h;  // visible: [lo, hi]
-            uint32_t u[2][32];
-            float mh = -INFINITY;
-            if (warp_active) {
-                ptx::tmem_ld32(scol, u[0]);
-                ptx::tmem_ld32(scol + 32, u[1]);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence32(u[0]);
-                ptx::reg_fence32(u[1]);
-                if (tid == 0) FA8_EV(0, it);
-                if (need_mask) {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        if (i > hi || i < lo) u[i >> 5][i & 31] = __float_as_uint(-INFINITY);
-                }
-                float mq[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t *v = &u[q >> 1][(q & 1) * 16];
-                    float m = ptx::fmax3(u2f(v[0]), u2f(v[1]), u2f(v[2]));
-#pragma unroll
-                    for (int i = 3; i < 15; i += 2) m = ptx::fmax3(m, u2f(v[i]), u2f(v[i + 1]));
-                    mq[q] = fmaxf(m, u2f(v[15]));
-                }
-                mh = fmaxf(ptx::fmax3(mq[0], mq[1], mq[2]), mq[3]);
-            }
-            // exchange the half-row maxima (double-buffered slots, bounded wait)
-            mx_part[((it & 1) * 2 + h) * 128 + r] = mh;
-            ptx::mbar_arrive(BAR(C::B_XCH + (it & 1)));
-            if (!W.wait_warp(BAR(C::B_XCH + (it & 1)), (uint32_t)(it >> 1) & 1u)) break;
-            const float mx = fmaxf(mh, mx_part[((it & 1) * 2 + (h ^ 1)) * 128 + r]);
-            if (tid == 0) FA8_EV(1, it);
-            float alpha = 1.f;
-            if (warp_active) {
-                const float mt = mx * c;
-                if (mt > m_run + kTau) {
-                    alpha = ptx::ex2(m_run - mt);
-                    row_sum *= alpha;
-                    m_run = mt;
-                }
-                const float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
-                const uint64_t b2 = ptx::f2pack(bias, bias);
-                uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
-                // P = 2^(s c - m + 8); the packed E4M3 of keys [32q, 32q+32) goes to column
-                // 32q of the S buffer (P_lo 8 columns later on masked tiles)
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    uint32_t w[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float x0, x1, x2, x3;
-                        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k]), u2f(u[g][4 * k + 1])), c2, b2), x0, x1);
-                        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k + 2]), u2f(u[g][4 * k + 3])), c2, b2), x2, x3);
-                        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
-                        acc0 = ptx::fadd2(acc0, ptx::f2pack(p0, p1));
-                        acc1 = ptx::fadd2(acc1, ptx::f2pack(p2, p3));
-                        w[k] = ptx::cvt_e4m3x2(p1, p0) | (ptx::cvt_e4m3x2(p3, p2) << 16);
-                        u[g][4 * k] = __float_as_uint(p0);
-                        u[g][4 * k + 1] = __float_as_uint(p1);
-                        u[g][4 * k + 2] = __float_as_uint(p2);
-                        u[g][4 * k + 3] = __float_as_uint(p3);
-                    }
-                    ptx::tmem_st8(scol + 32 * g, w);
-                    if (need_mask) {
-                        // second E4M3 term on masked tiles: P_lo = e4m3(p - P_hi)
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            float q0, q1, q2, q3;
-                            ptx::e4m3x2_to_f32(w[k] & 0xFFFFu, q0, q1);
-                            ptx::e4m3x2_to_f32(w[k] >> 16, q2, q3);
-                            w[k] = ptx::cvt_e4m3x2(u2f(u[g][4 * k + 1]) - q1, u2f(u[g][4 * k]) - q0) |
-                                   (ptx::cvt_e4m3x2(u2f(u[g][4 * k + 3]) - q3, u2f(u[g][4 * k + 2]) - q2) << 16);
-                        }
-                        ptx::tmem_st8(scol + 32 * g + 8, w);
-                    }
-                }
-                if (tid == 0) FA8_EV(13, it);
-                ptx::tmem_wait_st();
-                float a0, a1, a2, a3;
-                ptx::f2unpack(acc0, a0, a1);
-                ptx::f2unpack(acc1, a2, a3);
-                row_sum += (a0 + a1) + (a2 + a3);
-            }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(BAR(C::B_PF + sb));
-            if (tid == 0) FA8_EV(5, it);
-            if (h == 0) {
-                const int as = it % C::NA;
-                if (!W.wait_warp(BAR(C::B_AE + as), ((uint32_t)(it / C::NA) & 1u) ^ 1u)) break;
-                alpha_ring[as * 128 + r] = alpha;
-                ptx::mbar_arrive(BAR(C::B_AF + as));
-                if (tid == 0) FA8_EV(6, it);
-            }
-        }
-        // combine the two halves' row sums, then finalize: the 2^8 bias cancels between O
-        // and row_sum and is removed from the LSE
-        if (h == 1) {
-            sum_part[r] = row_sum;
-            ptx::mbar_arrive(BAR(C::B_SUM));
-        } else {
-            const bool got = W.wait_warp(BAR(C::B_SUM), 0);
-            row_sum += got ? sum_part[r] : 0.f;
-            const float dvv = p.dv ? p.dv[b * p.dv_sb + kvh * p.dv_sh] : 1.f;
-            float scale_o = 0.f, lse;
-            const float sig = has_sink ? p.sink[hq] : 0.f;
-            if (m_run == -INFINITY) {
-                lse = has_sink ? sig : -INFINITY;
-            } else {
-                const float sl2 = sig * kLog2e;
-                const float m_f = (has_sink && sl2 > m_run) ? sl2 : m_run;
-                const float sc = ptx::ex2(m_run - m_f);
-                const float rs = row_sum * sc + (has_sink ? ptx::ex2(sl2 - m_f + kPBias) : 0.f);
-                scale_o = sc * dvv / rs;
-                lse = (ptx::lg2(rs) + m_f - kPBias) * kLn2;
-            }
-            row_scale[r] = scale_o;
-            ptx::mbar_arrive(BAR(C::B_FIN));
-            if (row_ok) {
-                if (p.split_mode)
-                    p.lse_part[((long long)split * p.total_q + tok) * p.Hq + hq] = lse;
-                else if (p.lse)
-                    p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
-            }
-        }
-      }
-    } else {
-      ptx::setmaxnreg_inc<kRegsCorr>();
-      {
-        // ======================================================== correction (warps 8-11)
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const bool warp_active = __any_sync(0xffffffffu, row_ok);
-        float o[C::O_REGS ? DV : 1];
-#pragma unroll
-        for (int i = 0; i < (C::O_REGS ? DV : 1); ++i) o[i] = 0.f;
+        float alpha_prev = 0.f;
         int pv_uses = 0;
         bool ok = true;
-        for (int it = 0; ok && it < n_tiles; ++it) {
-            const int as = it % C::NA;
-            if (!W.wait_warp(BAR(C::B_AF + as), (uint32_t)(it / C::NA) & 1u)) break;
-            const float alpha = alpha_ring[as * 128 + r];
-            ptx::mbar_arrive(BAR(C::B_AE + as));
-#pragma unroll
-            for (int c = 0; c < C::NPV; ++c) {
-                const int ob = pv_uses % C::NOT;
-                if (!W.wait_warp(BAR(C::B_OF + ob), (uint32_t)(pv_uses / C::NOT) & 1u)) { ok = false; break; }
-                if (tid == 256 && c == 0) FA8_EV(7, it);
+        for (int it = 0; ok && it <= n_tiles; ++it) {
+            float alpha = 1.f;
+            if (it < n_tiles) {
+                // ------------------------------------------------ softmax of tile it
+                const int k0 = (t_beg + it) * kTileN;
+                const int sb = it % C::NS;
+                if (!W.wait_warp(BAR(C::B_SF + sb), (uint32_t)(it / C::NS) & 1u)) { ok = false; break; }
+                if (tid == 0) FA8_EV(4, it);
                 ptx::tc_fence_after();
-                const uint32_t otile = tmem + lane_base + C::TM_OT + ob * C::OTW;
+                const uint32_t scol = tmem + lane_base + C::TM_S + sb * 128 + 64 * h;
+                const bool need_mask = tile_needs_mask(k0, Lk, p.causal, p.window_left, pos0, pos_last, delta);
+                const int hi = hi_row - k0 - 64 * h, lo = lo_row - k0 - 64 * h;  // visible: [lo, hi]
+                uint32_t u[2][32];
+                float mh = -INFINITY;
                 if (warp_active) {
-                    if constexpr (C::O_REGS) {
-                        // one 32-column slice at a time, packed fold
-                        const uint64_t a2 = ptx::f2pack(alpha, alpha);
+                    ptx::tmem_ld32(scol, u[0]);
+                    ptx::tmem_ld32(scol + 32, u[1]);
+                    ptx::tmem_wait_ld();
+                    ptx::reg_fence32(u[0]);
+                    ptx::reg_fence32(u[1]);
+                    if (tid == 0) FA8_EV(0, it);
+                    if (need_mask) {
 #pragma unroll
-                        for (int j = 0; j < C::OTW / 32; ++j) {
-                            uint32_t u[32];
-                            ptx::tmem_ld32(otile + 32 * j, u);
-                            ptx::tmem_wait_ld();
-                            ptx::reg_fence32(u);
+                        for (int i = 0; i < 64; ++i)
+                            if (i > hi || i < lo) u[i >> 5][i & 31] = __float_as_uint(-INFINITY);
+                    }
+                    float mq[4];
 #pragma unroll
-                            for (int i = 0; i < 32; i += 2) {
-                                // O starts at 0 and the first visible tile has alpha = 0,
-                                // so no first-tile special case is needed
-                                const int idx = (C::O_REGS ? (32 * j + i) : 0);
-                                const uint64_t r2 = ptx::ffma2(ptx::f2pack(o[idx], o[idx + 1]), a2,
-                                                               ptx::f2pack(u2f(u[i]), u2f(u[i + 1])));
-                                ptx::f2unpack(r2, o[idx], o[idx + 1]);
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t *v = &u[q >> 1][(q & 1) * 16];
+                        float m = ptx::fmax3(u2f(v[0]), u2f(v[1]), u2f(v[2]));
+#pragma unroll
+                        for (int i = 3; i < 15; i += 2) m = ptx::fmax3(m, u2f(v[i]), u2f(v[i + 1]));
+                        mq[q] = fmaxf(m, u2f(v[15]));
+                    }
+                    mh = fmaxf(ptx::fmax3(mq[0], mq[1], mq[2]), mq[3]);
+                }
+                // exchange the half-row maxima (double-buffered slots, bounded wait)
+                mx_part[((it & 1) * 2 + h) * 128 + r] = mh;
+                ptx::mbar_arrive(BAR(C::B_XCH + (it & 1)));
+                if (!W.wait_warp(BAR(C::B_XCH + (it & 1)), (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
+                const float mx = fmaxf(mh, mx_part[((it & 1) * 2 + (h ^ 1)) * 128 + r]);
+                if (tid == 0) FA8_EV(1, it);
+                if (warp_active) {
+                    const float mt = mx * c;
+                    if (mt > m_run + kTau) {
+                        alpha = ptx::ex2(m_run - mt);
+                        row_sum *= alpha;
+                        m_run = mt;
+                    }
+                    const float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
+                    const uint64_t b2 = ptx::f2pack(bias, bias);
+                    uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
+                    // P = 2^(s c - m + 8); the packed E4M3 of keys [32q, 32q+32) goes to column
+                    // 32q of the S buffer (P_lo 8 columns later on masked tiles)
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        uint32_t w[8], wl[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            float x0, x1, x2, x3;
+                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k]), u2f(u[g][4 * k + 1])), c2, b2), x0, x1);
+                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k + 2]), u2f(u[g][4 * k + 3])), c2, b2), x2, x3);
+                            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
+                            acc0 = ptx::fadd2(acc0, ptx::f2pack(p0, p1));
+                            acc1 = ptx::fadd2(acc1, ptx::f2pack(p2, p3));
+                            const uint32_t h01 = ptx::cvt_e4m3x2(p1, p0), h23 = ptx::cvt_e4m3x2(p3, p2);
+                            w[k] = ptx::prmt_lo16(h01, h23);
+                            if (need_mask) {
+                                // second E4M3 term on masked tiles: P_lo = e4m3(p - P_hi)
+                                float q0, q1, q2, q3;
+                                ptx::e4m3x2_to_f32(h01, q0, q1);
+                                ptx::e4m3x2_to_f32(h23, q2, q3);
+                                wl[k] = ptx::prmt_lo16(ptx::cvt_e4m3x2(p1 - q1, p0 - q0), ptx::cvt_e4m3x2(p3 - q3, p2 - q2));
                             }
                         }
-                    } else {
+                        ptx::tmem_st8(scol + 32 * g, w);
+                        if (need_mask) ptx::tmem_st8(scol + 32 * g + 8, wl);
+                    }
+                    ptx::tmem_wait_st();
+                    float a0, a1, a2, a3;
+                    ptx::f2unpack(acc0, a0, a1);
+                    ptx::f2unpack(acc1, a2, a3);
+                    row_sum += (a0 + a1) + (a2 + a3);
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(BAR(C::B_PF + sb));
+                if (tid == 0) FA8_EV(5, it);
+            }
+            if (it > 0) {
+                // ------------------------------------------------ fold of tile it-1 (this half's columns)
 #pragma unroll
-                        for (int j = 0; j < C::OTW / 32; ++j) {
-                            uint32_t u[32];
-                            ptx::tmem_ld32(otile + 32 * j, u);
-                            const uint32_t orun = tmem + lane_base + C::TM_OR + c * C::OTW + 32 * j;
-                            uint32_t v[32];
-                            if (it > 0) {
+                for (int cc = 0; cc < C::NPV; ++cc) {
+                    const int ob = pv_uses % C::NOT;
+                    if (!W.wait_warp(BAR(C::B_OF + ob), (uint32_t)(pv_uses / C::NOT) & 1u)) { ok = false; break; }
+                    if (tid == 0 && cc == 0) FA8_EV(7, it - 1);
+                    ptx::tc_fence_after();
+                    const uint32_t otile = tmem + lane_base + C::TM_OT + ob * C::OTW + HOT * h;
+                    if (warp_active) {
+                        if constexpr (C::O_REGS) {
+                            // O starts at 0 and the first visible tile has alpha = 0
+                            const uint64_t a2 = ptx::f2pack(alpha_prev, alpha_prev);
+#pragma unroll
+                            for (int j = 0; j < HOT / 32; j += 2) {
+                                uint32_t t0[32], t1[32];
+                                ptx::tmem_ld32(otile + 32 * j, t0);
+                                if (j + 1 < HOT / 32) ptx::tmem_ld32(otile + 32 * (j + 1), t1);
+                                ptx::tmem_wait_ld();
+                                ptx::reg_fence32(t0);
+                                if (j + 1 < HOT / 32) ptx::reg_fence32(t1);
+#pragma unroll
+                                for (int hh = 0; hh < 2; ++hh) {
+                                    if (j + hh < HOT / 32) {
+                                        const uint32_t *t = hh ? t1 : t0;
+#pragma unroll
+                                        for (int i = 0; i < 32; i += 2) {
+                                            const int idx = C::O_REGS ? (32 * (j + hh) + i) : 0;
+                                            const uint64_t r2 = ptx::ffma2(ptx::f2pack(o[idx], o[idx + 1]), a2,
+                                                                           ptx::f2pack(u2f(t[i]), u2f(t[i + 1])));
+                                            ptx::f2unpack(r2, o[idx], o[idx + 1]);
+                                        }
+                                    }
+                                }
+                            }
+                        } else {
+                            // running O in TMEM: O_run[cols] = O_run * alpha + O_tile
+#pragma unroll 1
+                            for (int j = 0; j < HOT / 32; ++j) {
+                                const uint32_t orun = tmem + lane_base + C::TM_OR + cc * C::OTW + HOT * h + 32 * j;
+                                uint32_t t[32], v[32];
+                                ptx::tmem_ld32(otile + 32 * j, t);
                                 ptx::tmem_ld32(orun, v);
                                 ptx::tmem_wait_ld();
-                                ptx::reg_fence32(u);
+                                ptx::reg_fence32(t);
                                 ptx::reg_fence32(v);
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(fmaf(u2f(v[i]), alpha, u2f(u[i])));
-                            } else {
-                                ptx::tmem_wait_ld();
-                                ptx::reg_fence32(u);
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) v[i] = u[i];
+                                for (int i = 0; i < 32; ++i) {
+                                    // O_run is uninitialised before the first fold; a row's first
+                                    // visible tile has alpha = 0
+                                    const float prev = (it == 1 || alpha_prev == 0.f) ? 0.f : u2f(v[i]) * alpha_prev;
+                                    v[i] = __float_as_uint(prev + u2f(t[i]));
+                                }
+                                ptx::tmem_st32(orun, v);
                             }
-                            ptx::tmem_st32(orun, v);
                             ptx::tmem_wait_st();
                         }
                     }
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(BAR(C::B_OE + ob));
+                    if (tid == 0 && cc == C::NPV - 1) FA8_EV(8, it - 1);
+                    ++pv_uses;
                 }
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(BAR(C::B_OE + ob));
-                if (tid == 256 && c == C::NPV - 1) FA8_EV(8, it);
-                ++pv_uses;
             }
+            alpha_prev = alpha;
         }
-        const bool fin = W.wait_warp(BAR(C::B_FIN), 0);
-        const float sc = fin ? row_scale[r] : 0.f;
-        // TMEM loads are warp-collective (.sync.aligned): the whole active warp loads, only
-        // the valid rows store.
+        // ---------------------------------------------------- finalize: combine the halves'
+        // row sums; the 2^8 bias cancels between O and row_sum and is removed from the LSE
+        sum_part[h * 128 + r] = row_sum;
+        ptx::mbar_arrive(BAR(C::B_SUM));
+        const bool got = W.wait_warp(BAR(C::B_SUM), 0);
+        row_sum += got ? sum_part[(h ^ 1) * 128 + r] : 0.f;
+        const float dvv = p.dv ? p.dv[b * p.dv_sb + kvh * p.dv_sh] : 1.f;
+        float sc = 0.f, lse;
+        const float sig = has_sink ? p.sink[hq] : 0.f;
+        if (m_run == -INFINITY) {
+            lse = has_sink ? sig : -INFINITY;
+        } else {
+            const float sl2 = sig * kLog2e;
+            const float m_f = (has_sink && sl2 > m_run) ? sl2 : m_run;
+            const float scm = ptx::ex2(m_run - m_f);
+            const float rs = row_sum * scm + (has_sink ? ptx::ex2(sl2 - m_f + kPBias) : 0.f);
+            sc = scm * dvv / rs;
+            lse = (ptx::lg2(rs) + m_f - kPBias) * kLn2;
+        }
+        if (row_ok && h == 0) {
+            if (p.split_mode)
+                p.lse_part[((long long)split * p.total_q + tok) * p.Hq + hq] = lse;
+            else if (p.lse)
+                p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
+        }
+        // ---------------------------------------------------- store this half's O columns
+        // (TMEM loads are warp-collective: the whole active warp loads, valid rows store)
         if (warp_active) {
             if (p.split_mode) {
                 float *dst = p.o_part + (((long long)split * p.total_q + tok) * p.Hq + hq) * DV;
                 if constexpr (C::O_REGS) {
+                    dst += HDV * h;
                     if (row_ok) {
 #pragma unroll
-                        for (int i = 0; i < DV; i += 4)
+                        for (int i = 0; i < HDV; i += 4)
                             *reinterpret_cast<float4 *>(dst + i) =
                                 make_float4(o[i] * sc, o[i + 1] * sc, o[i + 2] * sc, o[i + 3] * sc);
                     }
                 } else {
 #pragma unroll 1
-                    for (int j = 0; j < DV / 32; ++j) {
+                    for (int j = 0; j < HDV / 32; ++j) {
                         uint32_t v[32];
-                        ptx::tmem_ld32(tmem + lane_base + C::TM_OR + 32 * j, v);
+                        ptx::tmem_ld32(tmem + lane_base + C::TM_OR + out_col<C>(h, j), v);
                         ptx::tmem_wait_ld();
                         ptx::reg_fence32(v);
                         if (row_ok) {
 #pragma unroll
                             for (int i = 0; i < 32; i += 4)
-                                *reinterpret_cast<float4 *>(dst + 32 * j + i) = make_float4(
+                                *reinterpret_cast<float4 *>(dst + out_col<C>(h, j) + i) = make_float4(
                                     u2f(v[i]) * sc, u2f(v[i + 1]) * sc, u2f(v[i + 2]) * sc, u2f(v[i + 3]) * sc);
                         }
                     }
@@ -863,9 +847,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             } else {
                 uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + 2 * (beta * p.o_sb + rho * p.o_ss + hq * p.o_sh);
                 if constexpr (C::O_REGS) {
+                    dst += 2 * HDV * h;
                     if (row_ok) {
 #pragma unroll
-                        for (int i = 0; i < DV; i += 8) {
+                        for (int i = 0; i < HDV; i += 8) {
                             float t8[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) t8[e] = o[i + e] * sc;
@@ -874,9 +859,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 } else {
 #pragma unroll 1
-                    for (int j = 0; j < DV / 32; ++j) {
+                    for (int j = 0; j < HDV / 32; ++j) {
                         uint32_t v[32];
-                        ptx::tmem_ld32(tmem + lane_base + C::TM_OR + 32 * j, v);
+                        ptx::tmem_ld32(tmem + lane_base + C::TM_OR + out_col<C>(h, j), v);
                         ptx::tmem_wait_ld();
                         ptx::reg_fence32(v);
                         if (row_ok) {
@@ -885,20 +870,28 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 float t8[8];
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) t8[e] = u2f(v[i + e]) * sc;
-                                store8(dst + 2 * (32 * j + i), t8, p.out_fp16);
+                                store8(dst + 2 * (out_col<C>(h, j) + i), t8, p.out_fp16);
                             }
                         }
                     }
                 }
             }
         }
-    }
+      }
     }
     // ------------------------------------------------------------ teardown
     ptx::tc_fence_before();
     __syncthreads();
+#ifdef FA8_TRACE
     if (tid == 0) FA8_EV(15, 1);
-    if (warp == 13) {
+    __syncthreads();
+    if (p.trace && blockIdx.y == 0 && blockIdx.x < kTraceCtas) {
+        const unsigned long long *src = reinterpret_cast<const unsigned long long *>(smem + C::OFF_TRACE);
+        for (int i = tid; i < kTraceEvents * kTraceTiles; i += kNumThreads)
+            p.trace[(size_t)blockIdx.x * kTraceEvents * kTraceTiles + i] = src[i];
+    }
+#endif
+    if (warp == 9) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::TM_COLS);
     }

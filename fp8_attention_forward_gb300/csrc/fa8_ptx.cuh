@@ -50,6 +50,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but lets the hardware suspend the thread for up to `hint_ns`
+// nanoseconds waiting for the phase (it resumes as soon as the phase completes), so a
+// waiting warp does not occupy issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -240,6 +255,13 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 template <int N>
 __device__ __forceinline__ void setmaxnreg_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// (lo & 0xFFFF) | (hi << 16) in one byte-permute
+__device__ __forceinline__ uint32_t prmt_lo16(uint32_t lo, uint32_t hi) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(d) : "r"(lo), "r"(hi));
+    return d;
 }
 
 // Unpacks two E4M3 bytes (bits 0..7 -> lo, 8..15 -> hi) to fp32, exactly.
