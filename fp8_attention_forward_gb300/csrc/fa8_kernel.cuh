@@ -3,16 +3,17 @@
 //
 // One CTA computes one 128-row Q tile: the rows are (query position, q-head) pairs of one
 // kv-head group, packed position-major (PackGQA), against the kv-head's keys, for one
-// split of the request's key range.  Roles (384 threads, three warpgroups):
-//   warps 0-3   half 0 of every row: keys [0, 64) of each tile and O columns [0, dv/2)
-//   warps 4-7   half 1 of the same rows: keys [64, 128) and O columns [dv/2, dv)
-//               (thread r of a half owns TMEM lane r = tile row r)
-//   warp 8      TMA producer (Q once, K/V tiles into S-stage rings)
-//   warp 9      MMA issuer (one elected lane) and TMEM owner
-//   warps 10-11 idle (the control warpgroup gives its registers to the two halves)
-// Each half does the softmax of its 64 keys and the two-level fold of its half of O; the
-// two halves exchange their row maxima once per tile (so both use the same running max
-// and rescale factor) and their row sums once at the end.
+// split of the request's key range.  Roles (512 threads, four warpgroups):
+//   warps 0-3   softmax, keys [0, 64) of every tile: thread r owns TMEM lane r = row r
+//   warps 4-7   softmax, keys [64, 128) of the same rows; the two halves exchange their
+//               row maxima once per tile and their row sums once at the end
+//   warps 8-11  correction: two-level PV fold into fp32 O, epilogue
+//   warp 12     TMA producer (Q once, K/V tiles into S-stage rings)
+//   warp 13     MMA issuer (lane 0) and TMEM owner
+//   warps 14-15 idle (the control warpgroup gives its registers to the correction)
+// Splitting each row over two warps halves the per-warp softmax work per tile, so the
+// softmax keeps pace with the tensor core; each half reads its 64 S columns from TMEM in a
+// single round trip per tile.
 //
 // Per 128-key tile t (sources: "[Cute,Fwd,Sm90] Native FP8 (E4M3 Q/K/V) forward for
 // Hopper", Design; "tml-fa4 PR #4", Summary and "Correctness fix over #1"):
@@ -41,9 +42,10 @@ namespace fa8 {
 
 constexpr int kTileM = 128;     // Q rows per CTA = TMEM lanes
 constexpr int kTileN = 128;     // keys per KV tile
-constexpr int kNumThreads = 384;
-// registers per thread after setmaxnreg; 256 x 224 + 128 x 48 <= 384 x 168 (launch)
-constexpr int kRegsMath = 224;
+constexpr int kNumThreads = 512;
+// registers per thread after setmaxnreg; 256 x 112 + 128 x 240 + 128 x 48 = 512 x 128 (launch)
+constexpr int kRegsSoft = 112;
+constexpr int kRegsCorr = 240;
 constexpr int kRegsCtl = 48;
 constexpr float kTau = 0.75f;   // lazy-rescale threshold, log2 units
 constexpr float kPBias = 8.0f;  // P carries a factor 2^8
@@ -157,16 +159,19 @@ struct Cfg {
     static constexpr int B_PF = B_SF + NS;
     static constexpr int B_OF = B_PF + NS;   // NOT slots
     static constexpr int B_OE = B_OF + NOT;  // NOT slots
-    static constexpr int B_XCH = B_OE + NOT;  // 2 slots: row-max exchange between the halves
-    static constexpr int B_SUM = B_XCH + 2;   // final partial row sums of both halves
-    static constexpr int B_DONE = B_SUM + 1;
+    static constexpr int NA = 4;             // alpha ring depth (softmax -> correction)
+    static constexpr int B_AF = B_OE + NOT;  // NA slots
+    static constexpr int B_AE = B_AF + NA;   // NA slots
+    static constexpr int B_XCH = B_AE + NA;  // 2 slots: row-max exchange between the halves
+    static constexpr int B_SUM = B_XCH + 2;  // half 1 -> half 0: final partial row sums
+    static constexpr int B_FIN = B_SUM + 1;  // half 0 -> correction: final O scale
+    static constexpr int B_DONE = B_FIN + 1;
     static constexpr int NUM_BARS = B_DONE + 1;
     static_assert(STAGES >= 2, "smem too small for two K/V stages");
     static_assert(NUM_BARS * 8 <= 512, "barrier area");
     static_assert(TM_OR + (O_REGS ? 0 : DV) <= TM_COLS, "TMEM budget");
     static_assert(OTW % CWV == 0 && OTW % 32 == 0 && OTW % 16 == 0 && OTW <= 256, "PV shape");
     static_assert(D % 32 == 0 && DV % 32 == 0, "head dims");
-    static_assert(OTW % 64 == 0, "each half folds a multiple of 32 columns of every O_tile chunk");
 };
 
 // UMMA shared-memory descriptor: start >>4 [0,14), LBO >>4 [16,30), SBO >>4 [32,46),
@@ -282,13 +287,6 @@ __device__ __forceinline__ bool varlen_slot(const FwdParams &p, int x, int &b, i
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
-// O column of the j-th 32-column slice owned by half h: half h folds columns
-// [c*OTW + h*OTW/2, c*OTW + (h+1)*OTW/2) of every O_tile chunk c.
-template <class C>
-__host__ __device__ constexpr int out_col(int h, int j) {
-    return (j / (C::OTW / 64)) * C::OTW + (C::OTW / 2) * h + (j % (C::OTW / 64)) * 32;
-}
-
 // Writes 8 consecutive output values (one 16-byte store) in bf16 or fp16.
 __device__ __forceinline__ void store8(void *dst, const float *v, int fp16) {
     uint4 pk;
@@ -401,8 +399,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc + 512);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 516);
-    float *mx_part = reinterpret_cast<float *>(misc + 1024);   // [2 parity][2 half][128]
-    float *sum_part = reinterpret_cast<float *>(misc + 3072);  // [2 half][128]
+    float *alpha_ring = reinterpret_cast<float *>(misc + 1024);  // [NA][128]
+    float *row_scale = reinterpret_cast<float *>(misc + 3072);   // [128]
+    float *mx_part = reinterpret_cast<float *>(misc + 3584);     // [2 parity][2 half][128]
+    float *sum_part = reinterpret_cast<float *>(misc + 5632);    // [128]
     const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
     const uint32_t sK = ptx::smem_u32(smem + C::OFF_K);
     const uint32_t sV = ptx::smem_u32(smem + C::OFF_V);
@@ -421,10 +421,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         for (int i = 0; i < C::NOT; ++i) {
             ptx::mbar_init(BAR(C::B_OF + i), 1);
-            ptx::mbar_init(BAR(C::B_OE + i), 256);
+            ptx::mbar_init(BAR(C::B_OE + i), 128);
+        }
+        for (int i = 0; i < C::NA; ++i) {
+            ptx::mbar_init(BAR(C::B_AF + i), 128);
+            ptx::mbar_init(BAR(C::B_AE + i), 128);
         }
         for (int i = 0; i < 2; ++i) ptx::mbar_init(BAR(C::B_XCH + i), 256);
-        ptx::mbar_init(BAR(C::B_SUM), 256);
+        ptx::mbar_init(BAR(C::B_SUM), 128);
+        ptx::mbar_init(BAR(C::B_FIN), 128);
         ptx::mbar_init(BAR(C::B_DONE), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -434,12 +439,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     for (int i = tid; i < kTraceEvents * kTraceTiles; i += kNumThreads)
         reinterpret_cast<unsigned long long *>(smem + C::OFF_TRACE)[i] = 0ull;
 #endif
-    if (warp == 8 && lane == 0) {
+    if (warp == 12 && lane == 0) {
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
     }
-    if (warp == 9) {
+    if (warp == 13) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TM_COLS);
         ptx::tmem_relinquish();
     }
@@ -450,9 +455,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const Waiter W{abort_flag, p.timeout_ns, p.status};
     if (tid == 0) FA8_EV(15, 0);
 
-    if (warp >= 8) {
+    if (warp >= 12) {
       ptx::setmaxnreg_dec<kRegsCtl>();
-      if (warp == 8) {
+      if (warp == 12) {
         // ======================================================== TMA producer
         const bool paged = p.kv_mode == 2;
         int issued_k = 0, issued_v = 0;
@@ -530,7 +535,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 W.drain(BAR(C::B_VF + i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u);
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ======================================================== MMA issuer
         // The whole warp runs this loop (uniform control flow); one elected lane issues the
         // tcgen05 operations.  Shared-memory descriptors are built once and advanced by
@@ -614,13 +619,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         W.drain(BAR(C::B_DONE), 0);
         __syncwarp();
       }
-    } else {
-      ptx::setmaxnreg_inc<kRegsMath>();
+    } else if (warp < 8) {
+      ptx::setmaxnreg_dec<kRegsSoft>();
       {
-        // ======================================================== softmax + fold (half h)
-        constexpr int HDV = DV / 2;   // O columns of this half
-        constexpr int HOT = C::OTW / 2;  // columns of each O_tile chunk folded by this half
-        const int h = warp >> 2;
+        // ======================================================== softmax (half h of each row)
+        const int h = warp >> 2;  // keys [64 h, 64 h + 64) of every tile
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const bool warp_active = __any_sync(0xffffffffu, row_ok);
         const float dqv = p.dq ? p.dq[b * p.dq_sb + kvh * p.dq_sh] : 1.f;
@@ -629,68 +632,78 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const uint64_t c2 = ptx::f2pack(c, c);
         const int hi_row = p.causal ? min(Lk - 1, rpos + delta) : Lk - 1;
         const int lo_row = p.window_left >= 0 ? max(0, rpos + delta - p.window_left) : 0;
-        float o[C::O_REGS ? HDV : 1];
-#pragma unroll
-        for (int i = 0; i < (C::O_REGS ? HDV : 1); ++i) o[i] = 0.f;
         float m_run = -INFINITY, row_sum = 0.f;  // identical m_run in both halves
-        float alpha_prev = 0.f;
-        int pv_uses = 0;
-        bool ok = true;
-        for (int it = 0; ok && it <= n_tiles; ++it) {
-            float alpha = 1.f;
-            if (it < n_tiles) {
-                // ------------------------------------------------ softmax of tile it
-                const int k0 = (t_beg + it) * kTileN;
-                const int sb = it % C::NS;
-                if (!W.wait_warp(BAR(C::B_SF + sb), (uint32_t)(it / C::NS) & 1u)) { ok = false; break; }
-                if (tid == 0) FA8_EV(4, it);
-                ptx::tc_fence_after();
-                const uint32_t scol = tmem + lane_base + C::TM_S + sb * 128 + 64 * h;
-                const bool need_mask = tile_needs_mask(k0, Lk, p.causal, p.window_left, pos0, pos_last, delta);
-                const int hi = hi_row - k0 - 64 * h, lo = lo_row - k0 - 64 * h;  // visible: [lo, hi]
-                uint32_t u[2][32];
-                float mh = -INFINITY;
-                if (warp_active) {
-                    ptx::tmem_ld32(scol, u[0]);
-                    ptx::tmem_ld32(scol + 32, u[1]);
-                    ptx::tmem_wait_ld();
-                    ptx::reg_fence32(u[0]);
-                    ptx::reg_fence32(u[1]);
-                    if (tid == 0) FA8_EV(0, it);
-                    if (need_mask) {
+        for (int it = 0; it < n_tiles; ++it) {
+            const int k0 = (t_beg + it) * kTileN;
+            const int sb = it % C::NS;
+            if (!W.wait_warp(BAR(C::B_SF + sb), (uint32_t)(it / C::NS) & 1u)) break;
+            if (tid == 0) FA8_EV(4, it);
+            ptx::tc_fence_after();
+            const uint32_t scol = tmem + lane_base + C::TM_S + sb * 128 + 64 * h;
+            const bool need_mask = tile_needs_mask(k0, Lk, p.causal, p.window_left, pos0, pos_last, delta);
+            const int hi = hi_row - k0 - 64 * h, lo = lo_row - k0 - 64 * h;  // visible: [lo, hi]
+            uint32_t u[2][32];
+            float mh = -INFINITY;
+            if (warp_active) {
+                ptx::tmem_ld32(scol, u[0]);
+                ptx::tmem_ld32(scol + 32, u[1]);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence32(u[0]);
+                ptx::reg_fence32(u[1]);
+                if (tid == 0) FA8_EV(0, it);
+                if (need_mask) {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            if (i > hi || i < lo) u[i >> 5][i & 31] = __float_as_uint(-INFINITY);
-                    }
-                    float mq[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t *v = &u[q >> 1][(q & 1) * 16];
-                        float m = ptx::fmax3(u2f(v[0]), u2f(v[1]), u2f(v[2]));
-#pragma unroll
-                        for (int i = 3; i < 15; i += 2) m = ptx::fmax3(m, u2f(v[i]), u2f(v[i + 1]));
-                        mq[q] = fmaxf(m, u2f(v[15]));
-                    }
-                    mh = fmaxf(ptx::fmax3(mq[0], mq[1], mq[2]), mq[3]);
+                    for (int i = 0; i < 64; ++i)
+                        if (i > hi || i < lo) u[i >> 5][i & 31] = __float_as_uint(-INFINITY);
                 }
-                // exchange the half-row maxima (double-buffered slots, bounded wait)
-                mx_part[((it & 1) * 2 + h) * 128 + r] = mh;
-                ptx::mbar_arrive(BAR(C::B_XCH + (it & 1)));
-                if (!W.wait_warp(BAR(C::B_XCH + (it & 1)), (uint32_t)(it >> 1) & 1u)) { ok = false; break; }
-                const float mx = fmaxf(mh, mx_part[((it & 1) * 2 + (h ^ 1)) * 128 + r]);
-                if (tid == 0) FA8_EV(1, it);
-                if (warp_active) {
-                    const float mt = mx * c;
-                    if (mt > m_run + kTau) {
-                        alpha = ptx::ex2(m_run - mt);
-                        row_sum *= alpha;
-                        m_run = mt;
+                float mq[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t *v = &u[q >> 1][(q & 1) * 16];
+                    float m = ptx::fmax3(u2f(v[0]), u2f(v[1]), u2f(v[2]));
+#pragma unroll
+                    for (int i = 3; i < 15; i += 2) m = ptx::fmax3(m, u2f(v[i]), u2f(v[i + 1]));
+                    mq[q] = fmaxf(m, u2f(v[15]));
+                }
+                mh = fmaxf(ptx::fmax3(mq[0], mq[1], mq[2]), mq[3]);
+            }
+            // Publish this half's tile max, then emit P speculatively with the running max;
+            // the partner's max is read afterwards.  Only when the combined max exceeds the
+            // running max by more than tau (both halves see the same values and decide
+            // alike) is P emitted again with the new max.
+            mx_part[((it & 1) * 2 + h) * 128 + r] = mh;
+            ptx::mbar_arrive(BAR(C::B_XCH + (it & 1)));
+            float alpha = 1.f;
+            const bool spec = warp_active && m_run != -INFINITY && mh * c <= m_run + kTau;
+            float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
+            float tsum = 0.f;
+            bool xch_ok = true;
+#pragma unroll 1
+            for (int pass = 0; pass < 2; ++pass) {
+                bool emit = spec;
+                if (pass == 1) {
+                    if (!W.wait_warp(BAR(C::B_XCH + (it & 1)), (uint32_t)(it >> 1) & 1u)) { xch_ok = false; break; }
+                    const float mx = fmaxf(mh, mx_part[((it & 1) * 2 + (h ^ 1)) * 128 + r]);
+                    if (tid == 0) FA8_EV(1, it);
+                    emit = false;
+                    if (warp_active) {
+                        const float mt = mx * c;
+                        if (mt > m_run + kTau) {
+                            alpha = ptx::ex2(m_run - mt);
+                            row_sum *= alpha;
+                            m_run = mt;
+                            bias = kPBias - m_run;
+                            emit = true;
+                        } else {
+                            emit = !spec;  // (cannot happen: a speculative miss implies a rescale)
+                        }
                     }
-                    const float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
+                }
+                if (emit) {
                     const uint64_t b2 = ptx::f2pack(bias, bias);
                     uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
-                    // P = 2^(s c - m + 8); the packed E4M3 of keys [32q, 32q+32) goes to column
-                    // 32q of the S buffer (P_lo 8 columns later on masked tiles)
+                    // P = 2^(s c - m + 8); the packed E4M3 of keys [32q, 32q+32) goes to
+                    // column 32q of the S buffer (P_lo 8 columns later on masked tiles)
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {
                         uint32_t w[8], wl[8];
@@ -715,131 +728,158 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         ptx::tmem_st8(scol + 32 * g, w);
                         if (need_mask) ptx::tmem_st8(scol + 32 * g + 8, wl);
                     }
-                    ptx::tmem_wait_st();
                     float a0, a1, a2, a3;
                     ptx::f2unpack(acc0, a0, a1);
                     ptx::f2unpack(acc1, a2, a3);
-                    row_sum += (a0 + a1) + (a2 + a3);
+                    tsum = (a0 + a1) + (a2 + a3);
                 }
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(BAR(C::B_PF + sb));
-                if (tid == 0) FA8_EV(5, it);
             }
-            if (it > 0) {
-                // ------------------------------------------------ fold of tile it-1 (this half's columns)
+            if (!xch_ok) break;
+            if (warp_active) {
+                ptx::tmem_wait_st();
+                row_sum += tsum;
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(BAR(C::B_PF + sb));
+            if (tid == 0) FA8_EV(5, it);
+            if (h == 0) {
+                const int as = it % C::NA;
+                if (!W.wait_warp(BAR(C::B_AE + as), ((uint32_t)(it / C::NA) & 1u) ^ 1u)) break;
+                alpha_ring[as * 128 + r] = alpha;
+                ptx::mbar_arrive(BAR(C::B_AF + as));
+                if (tid == 0) FA8_EV(6, it);
+            }
+        }
+        // combine the two halves' row sums, then finalize: the 2^8 bias cancels between O
+        // and row_sum and is removed from the LSE
+        if (h == 1) {
+            sum_part[r] = row_sum;
+            ptx::mbar_arrive(BAR(C::B_SUM));
+        } else {
+            const bool got = W.wait_warp(BAR(C::B_SUM), 0);
+            row_sum += got ? sum_part[r] : 0.f;
+            const float dvv = p.dv ? p.dv[b * p.dv_sb + kvh * p.dv_sh] : 1.f;
+            float scale_o = 0.f, lse;
+            const float sig = has_sink ? p.sink[hq] : 0.f;
+            if (m_run == -INFINITY) {
+                lse = has_sink ? sig : -INFINITY;
+            } else {
+                const float sl2 = sig * kLog2e;
+                const float m_f = (has_sink && sl2 > m_run) ? sl2 : m_run;
+                const float sc = ptx::ex2(m_run - m_f);
+                const float rs = row_sum * sc + (has_sink ? ptx::ex2(sl2 - m_f + kPBias) : 0.f);
+                scale_o = sc * dvv / rs;
+                lse = (ptx::lg2(rs) + m_f - kPBias) * kLn2;
+            }
+            row_scale[r] = scale_o;
+            ptx::mbar_arrive(BAR(C::B_FIN));
+            if (row_ok) {
+                if (p.split_mode)
+                    p.lse_part[((long long)split * p.total_q + tok) * p.Hq + hq] = lse;
+                else if (p.lse)
+                    p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
+            }
+        }
+      }
+    } else {
+      ptx::setmaxnreg_inc<kRegsCorr>();
+      {
+        // ======================================================== correction (warps 8-11)
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const bool warp_active = __any_sync(0xffffffffu, row_ok);
+        float o[C::O_REGS ? DV : 1];
 #pragma unroll
-                for (int cc = 0; cc < C::NPV; ++cc) {
-                    const int ob = pv_uses % C::NOT;
-                    if (!W.wait_warp(BAR(C::B_OF + ob), (uint32_t)(pv_uses / C::NOT) & 1u)) { ok = false; break; }
-                    if (tid == 0 && cc == 0) FA8_EV(7, it - 1);
-                    ptx::tc_fence_after();
-                    const uint32_t otile = tmem + lane_base + C::TM_OT + ob * C::OTW + HOT * h;
-                    if (warp_active) {
-                        if constexpr (C::O_REGS) {
-                            // O starts at 0 and the first visible tile has alpha = 0
-                            const uint64_t a2 = ptx::f2pack(alpha_prev, alpha_prev);
+        for (int i = 0; i < (C::O_REGS ? DV : 1); ++i) o[i] = 0.f;
+        int pv_uses = 0;
+        bool ok = true;
+        for (int it = 0; ok && it < n_tiles; ++it) {
+            const int as = it % C::NA;
+            if (!W.wait_warp(BAR(C::B_AF + as), (uint32_t)(it / C::NA) & 1u)) break;
+            const float alpha = alpha_ring[as * 128 + r];
+            ptx::mbar_arrive(BAR(C::B_AE + as));
 #pragma unroll
-                            for (int j = 0; j < HOT / 32; j += 2) {
-                                uint32_t t0[32], t1[32];
-                                ptx::tmem_ld32(otile + 32 * j, t0);
-                                if (j + 1 < HOT / 32) ptx::tmem_ld32(otile + 32 * (j + 1), t1);
-                                ptx::tmem_wait_ld();
-                                ptx::reg_fence32(t0);
-                                if (j + 1 < HOT / 32) ptx::reg_fence32(t1);
+            for (int c = 0; c < C::NPV; ++c) {
+                const int ob = pv_uses % C::NOT;
+                if (!W.wait_warp(BAR(C::B_OF + ob), (uint32_t)(pv_uses / C::NOT) & 1u)) { ok = false; break; }
+                if (tid == 256 && c == 0) FA8_EV(7, it);
+                ptx::tc_fence_after();
+                const uint32_t otile = tmem + lane_base + C::TM_OT + ob * C::OTW;
+                if (warp_active) {
+                    if constexpr (C::O_REGS) {
+                        // one 32-column slice at a time, packed fold
+                        const uint64_t a2 = ptx::f2pack(alpha, alpha);
 #pragma unroll
-                                for (int hh = 0; hh < 2; ++hh) {
-                                    if (j + hh < HOT / 32) {
-                                        const uint32_t *t = hh ? t1 : t0;
+                        for (int j = 0; j < C::OTW / 32; ++j) {
+                            uint32_t u[32];
+                            ptx::tmem_ld32(otile + 32 * j, u);
+                            ptx::tmem_wait_ld();
+                            ptx::reg_fence32(u);
 #pragma unroll
-                                        for (int i = 0; i < 32; i += 2) {
-                                            const int idx = C::O_REGS ? (32 * (j + hh) + i) : 0;
-                                            const uint64_t r2 = ptx::ffma2(ptx::f2pack(o[idx], o[idx + 1]), a2,
-                                                                           ptx::f2pack(u2f(t[i]), u2f(t[i + 1])));
-                                            ptx::f2unpack(r2, o[idx], o[idx + 1]);
-                                        }
-                                    }
-                                }
+                            for (int i = 0; i < 32; i += 2) {
+                                // O starts at 0 and the first visible tile has alpha = 0,
+                                // so no first-tile special case is needed
+                                const int idx = (C::O_REGS ? (32 * j + i) : 0);
+                                const uint64_t r2 = ptx::ffma2(ptx::f2pack(o[idx], o[idx + 1]), a2,
+                                                               ptx::f2pack(u2f(u[i]), u2f(u[i + 1])));
+                                ptx::f2unpack(r2, o[idx], o[idx + 1]);
                             }
-                        } else {
-                            // running O in TMEM: O_run[cols] = O_run * alpha + O_tile
-#pragma unroll 1
-                            for (int j = 0; j < HOT / 32; ++j) {
-                                const uint32_t orun = tmem + lane_base + C::TM_OR + cc * C::OTW + HOT * h + 32 * j;
-                                uint32_t t[32], v[32];
-                                ptx::tmem_ld32(otile + 32 * j, t);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < C::OTW / 32; ++j) {
+                            uint32_t u[32];
+                            ptx::tmem_ld32(otile + 32 * j, u);
+                            const uint32_t orun = tmem + lane_base + C::TM_OR + c * C::OTW + 32 * j;
+                            uint32_t v[32];
+                            if (it > 0) {
                                 ptx::tmem_ld32(orun, v);
                                 ptx::tmem_wait_ld();
-                                ptx::reg_fence32(t);
+                                ptx::reg_fence32(u);
                                 ptx::reg_fence32(v);
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) {
-                                    // O_run is uninitialised before the first fold; a row's first
-                                    // visible tile has alpha = 0
-                                    const float prev = (it == 1 || alpha_prev == 0.f) ? 0.f : u2f(v[i]) * alpha_prev;
-                                    v[i] = __float_as_uint(prev + u2f(t[i]));
-                                }
-                                ptx::tmem_st32(orun, v);
+                                for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(fmaf(u2f(v[i]), alpha, u2f(u[i])));
+                            } else {
+                                ptx::tmem_wait_ld();
+                                ptx::reg_fence32(u);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = u[i];
                             }
+                            ptx::tmem_st32(orun, v);
                             ptx::tmem_wait_st();
                         }
                     }
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(BAR(C::B_OE + ob));
-                    if (tid == 0 && cc == C::NPV - 1) FA8_EV(8, it - 1);
-                    ++pv_uses;
                 }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(BAR(C::B_OE + ob));
+                if (tid == 256 && c == C::NPV - 1) FA8_EV(8, it);
+                ++pv_uses;
             }
-            alpha_prev = alpha;
         }
-        // ---------------------------------------------------- finalize: combine the halves'
-        // row sums; the 2^8 bias cancels between O and row_sum and is removed from the LSE
-        sum_part[h * 128 + r] = row_sum;
-        ptx::mbar_arrive(BAR(C::B_SUM));
-        const bool got = W.wait_warp(BAR(C::B_SUM), 0);
-        row_sum += got ? sum_part[(h ^ 1) * 128 + r] : 0.f;
-        const float dvv = p.dv ? p.dv[b * p.dv_sb + kvh * p.dv_sh] : 1.f;
-        float sc = 0.f, lse;
-        const float sig = has_sink ? p.sink[hq] : 0.f;
-        if (m_run == -INFINITY) {
-            lse = has_sink ? sig : -INFINITY;
-        } else {
-            const float sl2 = sig * kLog2e;
-            const float m_f = (has_sink && sl2 > m_run) ? sl2 : m_run;
-            const float scm = ptx::ex2(m_run - m_f);
-            const float rs = row_sum * scm + (has_sink ? ptx::ex2(sl2 - m_f + kPBias) : 0.f);
-            sc = scm * dvv / rs;
-            lse = (ptx::lg2(rs) + m_f - kPBias) * kLn2;
-        }
-        if (row_ok && h == 0) {
-            if (p.split_mode)
-                p.lse_part[((long long)split * p.total_q + tok) * p.Hq + hq] = lse;
-            else if (p.lse)
-                p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
-        }
-        // ---------------------------------------------------- store this half's O columns
-        // (TMEM loads are warp-collective: the whole active warp loads, valid rows store)
+        const bool fin = W.wait_warp(BAR(C::B_FIN), 0);
+        const float sc = fin ? row_scale[r] : 0.f;
+        // TMEM loads are warp-collective (.sync.aligned): the whole active warp loads, only
+        // the valid rows store.
         if (warp_active) {
             if (p.split_mode) {
                 float *dst = p.o_part + (((long long)split * p.total_q + tok) * p.Hq + hq) * DV;
                 if constexpr (C::O_REGS) {
-                    dst += HDV * h;
                     if (row_ok) {
 #pragma unroll
-                        for (int i = 0; i < HDV; i += 4)
+                        for (int i = 0; i < DV; i += 4)
                             *reinterpret_cast<float4 *>(dst + i) =
                                 make_float4(o[i] * sc, o[i + 1] * sc, o[i + 2] * sc, o[i + 3] * sc);
                     }
                 } else {
 #pragma unroll 1
-                    for (int j = 0; j < HDV / 32; ++j) {
+                    for (int j = 0; j < DV / 32; ++j) {
                         uint32_t v[32];
-                        ptx::tmem_ld32(tmem + lane_base + C::TM_OR + out_col<C>(h, j), v);
+                        ptx::tmem_ld32(tmem + lane_base + C::TM_OR + 32 * j, v);
                         ptx::tmem_wait_ld();
                         ptx::reg_fence32(v);
                         if (row_ok) {
 #pragma unroll
                             for (int i = 0; i < 32; i += 4)
-                                *reinterpret_cast<float4 *>(dst + out_col<C>(h, j) + i) = make_float4(
+                                *reinterpret_cast<float4 *>(dst + 32 * j + i) = make_float4(
                                     u2f(v[i]) * sc, u2f(v[i + 1]) * sc, u2f(v[i + 2]) * sc, u2f(v[i + 3]) * sc);
                         }
                     }
@@ -847,10 +887,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             } else {
                 uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + 2 * (beta * p.o_sb + rho * p.o_ss + hq * p.o_sh);
                 if constexpr (C::O_REGS) {
-                    dst += 2 * HDV * h;
                     if (row_ok) {
 #pragma unroll
-                        for (int i = 0; i < HDV; i += 8) {
+                        for (int i = 0; i < DV; i += 8) {
                             float t8[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) t8[e] = o[i + e] * sc;
@@ -859,9 +898,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 } else {
 #pragma unroll 1
-                    for (int j = 0; j < HDV / 32; ++j) {
+                    for (int j = 0; j < DV / 32; ++j) {
                         uint32_t v[32];
-                        ptx::tmem_ld32(tmem + lane_base + C::TM_OR + out_col<C>(h, j), v);
+                        ptx::tmem_ld32(tmem + lane_base + C::TM_OR + 32 * j, v);
                         ptx::tmem_wait_ld();
                         ptx::reg_fence32(v);
                         if (row_ok) {
@@ -870,14 +909,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                 float t8[8];
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) t8[e] = u2f(v[i + e]) * sc;
-                                store8(dst + 2 * (out_col<C>(h, j) + i), t8, p.out_fp16);
+                                store8(dst + 2 * (32 * j + i), t8, p.out_fp16);
                             }
                         }
                     }
                 }
             }
         }
-      }
+    }
     }
     // ------------------------------------------------------------ teardown
     ptx::tc_fence_before();
@@ -891,7 +930,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             p.trace[(size_t)blockIdx.x * kTraceEvents * kTraceTiles + i] = src[i];
     }
 #endif
-    if (warp == 9) {
+    if (warp == 13) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::TM_COLS);
     }
