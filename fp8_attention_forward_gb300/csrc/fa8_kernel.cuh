@@ -699,7 +699,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         }
                     }
                 }
-                if (emit) {
+                // tcgen05.st is warp-collective: the warp emits if any of its rows needs to.
+                // A row that did not need this pass recomputes exactly the values it had; a
+                // row whose speculative pass-0 values were invalid always emits in pass 1.
+                if (__any_sync(0xffffffffu, emit)) {
                     const uint64_t b2 = ptx::f2pack(bias, bias);
                     uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
                     // P = 2^(s c - m + 8); the packed E4M3 of keys [32q, 32q+32) goes to
