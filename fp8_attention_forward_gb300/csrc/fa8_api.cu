@@ -20,6 +20,10 @@
 // one per device that loads the library; read and cleared by fa8_check().
 __device__ unsigned int g_fa8_status_word;
 
+// Split-KV partials of fa8_fwd_static_scratch: one array per device that loads the
+// library, shared by every call (see the header for the ordering rule).
+static __device__ __align__(256) unsigned char g_fa8_static_scratch[FA8_STATIC_SCRATCH_BYTES];
+
 namespace fa8 {
 
 __global__ void wait_probe_kernel(unsigned long long timeout_ns, unsigned int *status) {
@@ -98,6 +102,27 @@ fa8_status device_state(DeviceState **out) {
         d.ready = true;
     }
     *out = &d;
+    return FA8_SUCCESS;
+}
+
+// Device address of g_fa8_static_scratch on the current device, looked up on the first
+// request for each device.
+void *g_scratch_ptr[64];
+
+fa8_status static_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(FA8_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_fa8_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        if (!ptr) return fail(FA8_ERR_CUDA, "static scratch has no device address");
+        g_scratch_ptr[dev] = ptr;
+    }
+    *out = g_scratch_ptr[dev];
     return FA8_SUCCESS;
 }
 
@@ -663,6 +688,31 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
         if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     }
     return FA8_SUCCESS;
+}
+
+fa8_status fa8_fwd_static_scratch(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v,
+                                  const fa8_tensor *descale_q, const fa8_tensor *descale_k,
+                                  const fa8_tensor *descale_v, fa8_tensor *out, fa8_tensor *lse,
+                                  const fa8_tensor *cu_seqlens_q, const fa8_tensor *cu_seqlens_k,
+                                  const fa8_tensor *block_table, int page_size, int causal, int window_left,
+                                  const fa8_tensor *sink, float softmax_scale, int num_splits, void *stream) {
+    g_last_error.clear();
+    void *scratch = nullptr;
+    fa8_status st = static_scratch(&scratch);
+    if (st) return st;
+    int splits = 0;
+    size_t need = 0;
+    st = fa8_fwd_workspace_size(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, &splits,
+                                &need);
+    if (st) return st;
+    if (need > FA8_STATIC_SCRATCH_BYTES)
+        return fail(FA8_ERR_WORKSPACE,
+                    "split-KV partials (%d splits) need %zu bytes but the static scratch holds %zu; "
+                    "pass a smaller num_splits or call fa8_fwd with a workspace",
+                    splits, need, (size_t)FA8_STATIC_SCRATCH_BYTES);
+    return fa8_fwd(q, k, v, descale_q, descale_k, descale_v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table,
+                   page_size, causal, window_left, sink, softmax_scale, num_splits, scratch,
+                   FA8_STATIC_SCRATCH_BYTES, stream);
 }
 
 }  // extern "C"

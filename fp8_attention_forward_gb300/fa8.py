@@ -55,6 +55,9 @@ SIGNATURES = {
     "fa8_fwd_plan": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t),
                                     ctypes.POINTER(ctypes.c_int64)]),
+    "fa8_fwd_static_scratch": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, _P, ctypes.c_float, ctypes.c_int,
+                                              ctypes.c_void_p]),
     "fa8_check": (ctypes.c_int, [ctypes.c_void_p]),
     "fa8_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "fa8_debug_wait_probe": (ctypes.c_int, [ctypes.c_void_p]),
@@ -167,6 +170,27 @@ def fwd(q, k, v, *, descale_q=None, descale_k=None, descale_v=None, out=None, ls
                        int(bool(causal)), int(window_left), _ref(views["sink"]), float(softmax_scale),
                        int(num_splits), ws_ptr, ws_bytes,
                        _stream_handle(stream, dev) if dev.type == "cuda" else ctypes.c_void_p(0))
+    _raise(st)
+    return out, lse
+
+
+STATIC_SCRATCH_BYTES = 32 * 1024 * 1024  # FA8_STATIC_SCRATCH_BYTES
+
+
+def fwd_static_scratch(q, k, v, *, out, lse=None, descale_q=None, descale_k=None, descale_v=None,
+                       cu_seqlens_q=None, cu_seqlens_k=None, block_table=None, page_size=0, causal=False,
+                       window_left=-1, sink=None, softmax_scale=0.0, num_splits=0, stream=None):
+    """``fa8_fwd_static_scratch``: the forward with split partials in the library's static
+    device scratch.  ``out`` (and ``lse`` if wanted) are caller-provided; nothing is allocated."""
+    views = dict(q=_view(q), k=_view(k), v=_view(v), dq=_view(descale_q), dk=_view(descale_k),
+                 dv=_view(descale_v), out=_view(out), lse=_view(lse), cq=_view(cu_seqlens_q),
+                 ck=_view(cu_seqlens_k), bt=_view(block_table), sink=_view(sink))
+    st = lib().fa8_fwd_static_scratch(_ref(views["q"]), _ref(views["k"]), _ref(views["v"]), _ref(views["dq"]),
+                                      _ref(views["dk"]), _ref(views["dv"]), _ref(views["out"]),
+                                      _ref(views["lse"]), _ref(views["cq"]), _ref(views["ck"]),
+                                      _ref(views["bt"]), int(page_size), int(bool(causal)), int(window_left),
+                                      _ref(views["sink"]), float(softmax_scale), int(num_splits),
+                                      _stream_handle(stream, q.device))
     _raise(st)
     return out, lse
 

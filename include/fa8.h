@@ -140,6 +140,44 @@ FA8_API fa8_status fa8_fwd_plan(const fa8_tensor *q, const fa8_tensor *k, const 
                                 int64_t *grid_out);
 
 /*
+ * fa8_fwd_static_scratch -- fa8_fwd without a caller-provided workspace.  The attention
+ * it computes is fa8_fwd's, argument for argument; nothing in the published method
+ * corresponds to this entry point, which only changes where the split partials live.
+ *
+ * Who it is for: callers that cannot hand the library a device buffer -- a runtime whose
+ * device memory is carved up once at start-up and that may not allocate afterwards, or
+ * plain C code that links only this library and has no allocator of its own.  Neither
+ * this function nor anything it calls allocates or frees device memory.
+ *
+ * Where the partials go: one array of FA8_STATIC_SCRATCH_BYTES (32 MiB) of device memory
+ * that the library declares statically, so it exists once per device for as long as the
+ * library is loaded.  A call whose split plan (see fa8_fwd_workspace_size) needs more
+ * than that returns FA8_ERR_WORKSPACE before anything is enqueued; lower num_splits or
+ * use fa8_fwd with a workspace of your own.  Calls whose plan has one split do not touch
+ * the array.  Nothing in it has to start at zero: every call writes each partial before
+ * the merge kernel reads it.
+ *
+ * Sharing: every call on a device uses the same array.  Two calls that can run at the
+ * same time on one device (different streams without an event between them, or different
+ * host threads) overwrite each other's partials and give wrong results; order them on one
+ * stream, or use fa8_fwd with separate workspaces.
+ *
+ * Set-up: the first call on each device, made with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and keeps it; make that first call
+ * before capturing a stream.  A failure there returns FA8_ERR_CUDA.
+ */
+#define FA8_STATIC_SCRATCH_BYTES ((size_t)32 * 1024 * 1024)
+FA8_API fa8_status fa8_fwd_static_scratch(const fa8_tensor *q, const fa8_tensor *k,
+                                          const fa8_tensor *v, const fa8_tensor *descale_q,
+                                          const fa8_tensor *descale_k,
+                                          const fa8_tensor *descale_v, fa8_tensor *out,
+                                          fa8_tensor *lse, const fa8_tensor *cu_seqlens_q,
+                                          const fa8_tensor *cu_seqlens_k,
+                                          const fa8_tensor *block_table, int page_size,
+                                          int causal, int window_left, const fa8_tensor *sink,
+                                          float softmax_scale, int num_splits, void *stream);
+
+/*
  * fa8_check -- synchronises `stream`, then reads and clears the library's device status
  * word for the current device: FA8_SUCCESS, FA8_ERR_DEVICE_TIMEOUT (a kernel gave up a
  * bounded wait and returned early; its outputs are undefined) or FA8_ERR_DEVICE_BOUNDS.
