@@ -104,10 +104,11 @@ def _barrier(world):
         torch.distributed.barrier()
 
 
-def _max_over_ranks(x: float, world: int) -> float:
+def _max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """The slowest rank's figure: replicas run independently and the job ends with the last."""
     if world == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 

@@ -1,0 +1,185 @@
+"""The C ABI without a GPU: the library loads, exports every function include/fa8.h
+declares, validates arguments on the host, and plans launches from shapes and the SM count
+alone.  A call that would need the device fails loudly (FA8_ERR_CUDA), never silently."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from fp8_attention_forward_gb300 import build, fa8
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa8.h")
+E4M3 = torch.float8_e4m3fn
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fa8.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"FA8_API\s+[\w\s\*]*?\b(fa8_\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("fa8_fwd", "fa8_fwd_workspace_size", "fa8_fwd_plan", "fa8_check", "fa8_last_error"):
+        assert n in names
+    assert len(names) == len(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    exported = subprocess.run(["nm", "-D", "--defined-only", fa8.LIB_PATH], capture_output=True,
+                              text=True, check=True).stdout
+    dyn = {line.split()[-1] for line in exported.splitlines() if " T " in line}
+    missing = [n for n in declared_functions() if n not in dyn]
+    assert not missing, missing
+    # nothing but the declared API is exported from the library's own code
+    extra = sorted(n for n in dyn if n.startswith("fa8_") and n not in declared_functions())
+    assert not extra, extra
+
+
+def test_binding_covers_the_header(lib):
+    assert set(declared_functions()) == set(fa8.SIGNATURES)
+    for n in declared_functions():
+        assert getattr(lib, n) is not None
+
+
+def test_status_strings_and_version(lib):
+    assert lib.fa8_version() == 100
+    for st, word in [(0, b"success"), (1, b"invalid"), (2, b"unsupported"), (3, b"workspace"),
+                     (4, b"CUDA"), (5, b"timed out"), (6, b"out of range"), (99, b"unknown")]:
+        assert word in lib.fa8_status_string(st)
+
+
+def test_wait_timeout_bounds(lib):
+    assert lib.fa8_set_wait_timeout_ns(10) == fa8.FA8_ERR_INVALID_ARG
+    assert b"timeout" in lib.fa8_last_error()
+    assert lib.fa8_set_wait_timeout_ns(2_000_000_000) == fa8.FA8_SUCCESS
+
+
+# ------------------------------------------------------------------ host-only planner
+def qkv(B=2, Sq=333, Sk=333, Hq=32, Hkv=8, D=128, DV=128, dtype=E4M3):
+    q = torch.zeros((B, Sq, Hq, D), dtype=torch.uint8).view(dtype)
+    k = torch.zeros((B, Sk, Hkv, D), dtype=torch.uint8).view(dtype)
+    v = torch.zeros((B, Sk, Hkv, DV), dtype=torch.uint8).view(dtype)
+    return q, k, v
+
+
+def plan(q, k, v, sm=152, **kw):
+    return fa8.plan(q, k, v, sm_count=sm, **kw)
+
+
+def test_plan_prefill_packs_gqa_rows(lib):
+    # G = 4 q-heads per kv-head -> 32 positions x 4 heads per 128-row tile
+    splits, ws, grid = plan(*qkv(B=2, Sq=4096, Sk=4096))
+    assert splits == 1 and ws == 0
+    assert grid == (2 * (4096 // 32), 8)
+
+
+def test_plan_decode_splits_and_workspace(lib):
+    B, Hq, Hkv, D = 64, 64, 8, 128
+    q = torch.zeros((B, 1, Hq, D), dtype=torch.uint8).view(E4M3)
+    kp = torch.zeros((4096, 16, Hkv, D), dtype=torch.uint8).view(E4M3)
+    bt = torch.zeros((B, 2048), dtype=torch.int32)
+    cu = torch.zeros((B + 1,), dtype=torch.int32)
+    splits, ws, grid = plan(q, kp, kp, cu_seqlens_k=cu, block_table=bt, page_size=16)
+    # 64 requests x 8 kv-heads = 512 CTAs < 8 x 152: split 3 ways
+    assert splits == 3
+    rows = B * Hq * splits
+    o_bytes = (rows * D * 4 + 255) // 256 * 256
+    assert ws == o_bytes + (rows * 4 + 255) // 256 * 256
+    assert grid == (B, Hkv * splits)
+    # an explicit split count is capped by the number of key tiles
+    s2, _, _ = plan(q, kp, kp, cu_seqlens_k=cu, block_table=bt, page_size=16, num_splits=4096)
+    assert s2 == 2048 * 16 // 128
+    # and 1 disables splitting
+    assert plan(q, kp, kp, cu_seqlens_k=cu, block_table=bt, page_size=16, num_splits=1)[0] == 1
+
+
+def test_plan_depends_on_sm_count_only_through_the_split_heuristic(lib):
+    q, k, v = qkv(B=1, Sq=1, Sk=65536, Hq=8, Hkv=1, D=256, DV=256)
+    a = plan(q, k, v, sm=152)
+    b = plan(q, k, v, sm=76)
+    assert a[2][0] == b[2][0] == 1
+    assert a[0] == 64 and b[0] == 64  # capped at 64 splits
+    c = plan(*qkv(B=1, Sq=1, Sk=1024, Hq=8, Hkv=1, D=256, DV=256), sm=152)
+    assert c[0] == 4  # 8 key tiles -> at most half as many splits
+
+
+def test_plan_varlen_slots(lib):
+    q = torch.zeros((1000, 16, 192), dtype=torch.uint8).view(E4M3)
+    k = torch.zeros((3000, 4, 192), dtype=torch.uint8).view(E4M3)
+    v = torch.zeros((3000, 4, 128), dtype=torch.uint8).view(E4M3)
+    cu = torch.tensor([0, 100, 1000], dtype=torch.int32)
+    cuk = torch.tensor([0, 1000, 3000], dtype=torch.int32)
+    splits, ws, grid = plan(q, k, v, cu_seqlens_q=cu, cu_seqlens_k=cuk)
+    # 32 positions per tile; one extra slot per request for tiles that straddle requests
+    assert grid == ((1000 + 31) // 32 + 2, 4 * splits)
+
+
+@pytest.mark.parametrize("mutate,status,needle", [
+    (lambda q, k, v: (q.view(torch.uint8).view(torch.float8_e5m2), k.view(torch.uint8).view(torch.float8_e5m2),
+                      v.view(torch.uint8).view(torch.float8_e5m2)), 2, "E5M2"),
+    (lambda q, k, v: (q, k, v.view(torch.uint8).view(torch.float8_e5m2)), 2, "E5M2"),
+    (lambda q, k, v: (q.view(torch.uint8).view(torch.bfloat16), k.view(torch.uint8).view(torch.bfloat16),
+                      v.view(torch.uint8).view(torch.bfloat16)), 2, "E4M3"),
+    (lambda q, k, v: (q[..., :80], k[..., :80], v[..., :80]), 2, "not supported"),
+    (lambda q, k, v: (q[:, :, :30], k, v), 1, "multiple of kv heads"),
+    (lambda q, k, v: (q, k[:1], v[:1]), 1, "batch"),
+    (lambda q, k, v: (q, k, v[:, :5]), 1, "leading shapes"),
+    (lambda q, k, v: (q[..., 8:], k[..., 8:], v[..., 8:]), 1, None),  # misaligned (and d=120)
+])
+def test_plan_rejects_bad_shapes(lib, mutate, status, needle):
+    q, k, v = mutate(*qkv())
+    with pytest.raises(fa8.Fa8Error) as ei:
+        plan(q, k, v)
+    assert ei.value.status in (status, 1, 2)
+    assert ei.value.status == status or needle is None
+    if needle:
+        assert needle in str(ei.value)
+
+
+def test_paged_plan_validation(lib):
+    q = torch.zeros((2, 1, 8, 128), dtype=torch.uint8).view(E4M3)
+    kp = torch.zeros((64, 16, 2, 128), dtype=torch.uint8).view(E4M3)
+    cu = torch.zeros((3,), dtype=torch.int32)
+    bt = torch.zeros((2, 8), dtype=torch.int32)
+    with pytest.raises(fa8.Fa8Error, match="page_size"):
+        plan(q, kp, kp, cu_seqlens_k=cu, block_table=bt, page_size=32)
+    with pytest.raises(fa8.Fa8Error, match="cu_seqlens_k"):
+        plan(q, kp, kp, block_table=bt, page_size=16)
+    with pytest.raises(fa8.Fa8Error, match="block_table rows"):
+        plan(q, kp, kp, cu_seqlens_k=cu, block_table=bt[:1], page_size=16)
+    kp12 = torch.zeros((64, 12, 2, 128), dtype=torch.uint8).view(E4M3)
+    with pytest.raises(fa8.Fa8Error, match="multiple of 8"):
+        plan(q, kp12, kp12, cu_seqlens_k=cu, block_table=bt, page_size=12)
+
+
+# ------------------------------------------------------------------ no silent CPU path
+def test_forward_without_a_device_fails_loudly(lib):
+    if torch.cuda.is_available():
+        pytest.skip("checks the behaviour without a CUDA device")
+    q, k, v = qkv(B=1, Sq=8, Sk=8, Hq=2, Hkv=2)
+    out = torch.zeros((1, 8, 2, 128), dtype=torch.bfloat16)
+    with pytest.raises(fa8.Fa8Error) as ei:
+        fa8.fwd(q, k, v, out=out, workspace=torch.zeros(16, dtype=torch.uint8))
+    assert ei.value.status == fa8.FA8_ERR_CUDA
+    assert bool((out == 0).all())
+
+
+def test_forward_validates_before_touching_the_device(lib):
+    q, k, v = qkv(B=1, Sq=8, Sk=8, Hq=2, Hkv=2)
+    out = torch.zeros((1, 8, 2, 64), dtype=torch.bfloat16)  # wrong dv
+    with pytest.raises(fa8.Fa8Error) as ei:
+        fa8.fwd(q, k, v, out=out, workspace=torch.zeros(16, dtype=torch.uint8))
+    assert ei.value.status == fa8.FA8_ERR_INVALID_ARG and "dv" in str(ei.value)
+    out = torch.zeros((1, 8, 2, 128), dtype=torch.float32)
+    with pytest.raises(fa8.Fa8Error, match="bf16 or fp16"):
+        fa8.fwd(q, k, v, out=out, workspace=torch.zeros(16, dtype=torch.uint8))
