@@ -202,8 +202,9 @@ __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatil
                                           unsigned long long timeout, unsigned int *status) {
     const uint64_t t0 = ptx::globaltimer();
     while (true) {
-        // sleeps in hardware (up to 20 us per try) instead of spinning on issue slots
-        if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (ptx::globaltimer() - t0 > timeout) {
             *abort = 1;
@@ -667,80 +668,62 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 }
                 mh = fmaxf(ptx::fmax3(mq[0], mq[1], mq[2]), mq[3]);
             }
-            // Publish this half's tile max, then emit P speculatively with the running max;
-            // the partner's max is read afterwards.  Only when the combined max exceeds the
-            // running max by more than tau (both halves see the same values and decide
-            // alike) is P emitted again with the new max.
+            // exchange the half-row maxima (double-buffered slots, bounded wait)
             mx_part[((it & 1) * 2 + h) * 128 + r] = mh;
             ptx::mbar_arrive(BAR(C::B_XCH + (it & 1)));
+            if (!W.wait_warp(BAR(C::B_XCH + (it & 1)), (uint32_t)(it >> 1) & 1u)) break;
+            const float mx = fmaxf(mh, mx_part[((it & 1) * 2 + (h ^ 1)) * 128 + r]);
+            if (tid == 0) FA8_EV(1, it);
             float alpha = 1.f;
-            const bool spec = warp_active && m_run != -INFINITY && mh * c <= m_run + kTau;
-            float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
-            float tsum = 0.f;
-            bool xch_ok = true;
-#pragma unroll 1
-            for (int pass = 0; pass < 2; ++pass) {
-                bool emit = spec;
-                if (pass == 1) {
-                    if (!W.wait_warp(BAR(C::B_XCH + (it & 1)), (uint32_t)(it >> 1) & 1u)) { xch_ok = false; break; }
-                    const float mx = fmaxf(mh, mx_part[((it & 1) * 2 + (h ^ 1)) * 128 + r]);
-                    if (tid == 0) FA8_EV(1, it);
-                    emit = false;
-                    if (warp_active) {
-                        const float mt = mx * c;
-                        if (mt > m_run + kTau) {
-                            alpha = ptx::ex2(m_run - mt);
-                            row_sum *= alpha;
-                            m_run = mt;
-                            bias = kPBias - m_run;
-                            emit = true;
-                        } else {
-                            emit = !spec;  // (cannot happen: a speculative miss implies a rescale)
-                        }
-                    }
+            if (warp_active) {
+                const float mt = mx * c;
+                if (mt > m_run + kTau) {
+                    alpha = ptx::ex2(m_run - mt);
+                    row_sum *= alpha;
+                    m_run = mt;
                 }
-                // tcgen05.st is warp-collective: the warp emits if any of its rows needs to.
-                // A row that did not need this pass recomputes exactly the values it had; a
-                // row whose speculative pass-0 values were invalid always emits in pass 1.
-                if (__any_sync(0xffffffffu, emit)) {
-                    const uint64_t b2 = ptx::f2pack(bias, bias);
-                    uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
-                    // P = 2^(s c - m + 8); the packed E4M3 of keys [32q, 32q+32) goes to
-                    // column 32q of the S buffer (P_lo 8 columns later on masked tiles)
+                const float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
+                const uint64_t b2 = ptx::f2pack(bias, bias);
+                uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
+                // P = 2^(s c - m + 8); the packed E4M3 of keys [32q, 32q+32) goes to column
+                // 32q of the S buffer (P_lo 8 columns later on masked tiles)
 #pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        uint32_t w[8], wl[8];
+                for (int g = 0; g < 2; ++g) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        float x0, x1, x2, x3;
+                        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k]), u2f(u[g][4 * k + 1])), c2, b2), x0, x1);
+                        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k + 2]), u2f(u[g][4 * k + 3])), c2, b2), x2, x3);
+                        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
+                        acc0 = ptx::fadd2(acc0, ptx::f2pack(p0, p1));
+                        acc1 = ptx::fadd2(acc1, ptx::f2pack(p2, p3));
+                        w[k] = ptx::cvt_e4m3x2(p1, p0) | (ptx::cvt_e4m3x2(p3, p2) << 16);
+                        u[g][4 * k] = __float_as_uint(p0);
+                        u[g][4 * k + 1] = __float_as_uint(p1);
+                        u[g][4 * k + 2] = __float_as_uint(p2);
+                        u[g][4 * k + 3] = __float_as_uint(p3);
+                    }
+                    ptx::tmem_st8(scol + 32 * g, w);
+                    if (need_mask) {
+                        // second E4M3 term on masked tiles: P_lo = e4m3(p - P_hi)
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
-                            float x0, x1, x2, x3;
-                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k]), u2f(u[g][4 * k + 1])), c2, b2), x0, x1);
-                            ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k + 2]), u2f(u[g][4 * k + 3])), c2, b2), x2, x3);
-                            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
-                            acc0 = ptx::fadd2(acc0, ptx::f2pack(p0, p1));
-                            acc1 = ptx::fadd2(acc1, ptx::f2pack(p2, p3));
-                            const uint32_t h01 = ptx::cvt_e4m3x2(p1, p0), h23 = ptx::cvt_e4m3x2(p3, p2);
-                            w[k] = ptx::prmt_lo16(h01, h23);
-                            if (need_mask) {
-                                // second E4M3 term on masked tiles: P_lo = e4m3(p - P_hi)
-                                float q0, q1, q2, q3;
-                                ptx::e4m3x2_to_f32(h01, q0, q1);
-                                ptx::e4m3x2_to_f32(h23, q2, q3);
-                                wl[k] = ptx::prmt_lo16(ptx::cvt_e4m3x2(p1 - q1, p0 - q0), ptx::cvt_e4m3x2(p3 - q3, p2 - q2));
-                            }
+                            float q0, q1, q2, q3;
+                            ptx::e4m3x2_to_f32(w[k] & 0xFFFFu, q0, q1);
+                            ptx::e4m3x2_to_f32(w[k] >> 16, q2, q3);
+                            w[k] = ptx::cvt_e4m3x2(u2f(u[g][4 * k + 1]) - q1, u2f(u[g][4 * k]) - q0) |
+                                   (ptx::cvt_e4m3x2(u2f(u[g][4 * k + 3]) - q3, u2f(u[g][4 * k + 2]) - q2) << 16);
                         }
-                        ptx::tmem_st8(scol + 32 * g, w);
-                        if (need_mask) ptx::tmem_st8(scol + 32 * g + 8, wl);
+                        ptx::tmem_st8(scol + 32 * g + 8, w);
                     }
-                    float a0, a1, a2, a3;
-                    ptx::f2unpack(acc0, a0, a1);
-                    ptx::f2unpack(acc1, a2, a3);
-                    tsum = (a0 + a1) + (a2 + a3);
                 }
-            }
-            if (!xch_ok) break;
-            if (warp_active) {
+                if (tid == 0) FA8_EV(13, it);
                 ptx::tmem_wait_st();
-                row_sum += tsum;
+                float a0, a1, a2, a3;
+                ptx::f2unpack(acc0, a0, a1);
+                ptx::f2unpack(acc1, a2, a3);
+                row_sum += (a0 + a1) + (a2 + a3);
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(BAR(C::B_PF + sb));
