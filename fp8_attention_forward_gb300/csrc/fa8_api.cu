@@ -61,6 +61,7 @@ namespace {
 thread_local std::string g_last_error;
 unsigned long long g_timeout_ns = 2000000000ull;
 unsigned long long *g_trace = nullptr;  // pipeline trace buffer (FA8_TRACE builds)
+bool g_decode_kernel = true;            // few-rows shapes go to decode_kernel
 
 fa8_status fail(fa8_status s, const char *fmt, ...) {
     char buf[512];
@@ -189,6 +190,7 @@ struct Plan {
     int splits = 1;
     long long max_lk = 0;
     size_t ws_bytes = 0;
+    int decode = 0;  // launch decode_kernel (at most 16 rows per kv-head, dv % 128 == 0)
 };
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -249,6 +251,13 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
     if (p.G > 128) return fail(FA8_ERR_UNSUPPORTED, "more than 128 q-heads per kv-head (%d)", p.G);
     p.P = 128 / p.G;
     p.rows_per_tile = p.P * p.G;
+    // Decode shapes: batched q whose rows per kv-head (Sq x G) fit one 16-row tile.
+    if (g_decode_kernel && q->ndim == 4 && p.DV % 128 == 0 && 16 % p.G == 0 && q->shape[1] * p.G <= 16 &&
+        q->shape[1] > 0) {
+        p.decode = 1;
+        p.P = 16 / p.G;
+        p.rows_per_tile = 16;
+    }
 
     // ---- Q layout
     if (q->ndim == 4) {
@@ -374,6 +383,13 @@ const char *fa8_status_string(fa8_status s) {
         case FA8_ERR_DEVICE_BOUNDS: return "device index out of range";
     }
     return "unknown status";
+}
+
+fa8_status fa8_set_decode_kernel(int enable) {
+    g_last_error.clear();
+    if (enable != 0 && enable != 1) return fail(FA8_ERR_INVALID_ARG, "enable must be 0 or 1");
+    g_decode_kernel = enable == 1;
+    return FA8_SUCCESS;
 }
 
 fa8_status fa8_set_wait_timeout_ns(uint64_t ns) {
@@ -651,7 +667,14 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
     const dim3 grid((unsigned)pl.num_slots, (unsigned)(pl.Hkv * pl.splits), 1);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    switch (pl.D * 1000 + pl.DV) {
+    if (pl.decode) {
+        switch (pl.D * 1000 + pl.DV) {
+            case 128128: e = fa8::launch_decode<128, 128>(p, tq, tk, tv, grid, s); break;
+            case 192128: e = fa8::launch_decode<192, 128>(p, tq, tk, tv, grid, s); break;
+            case 256256: e = fa8::launch_decode<256, 256>(p, tq, tk, tv, grid, s); break;
+            default: return fail(FA8_ERR_UNSUPPORTED, "no decode kernel for (%d, %d)", pl.D, pl.DV);
+        }
+    } else switch (pl.D * 1000 + pl.DV) {
         case 64064: e = fa8::launch_fwd<64, 64>(p, tq, tk, tv, grid, s); break;
         case 128128: e = fa8::launch_fwd<128, 128>(p, tq, tk, tv, grid, s); break;
         case 192128: e = fa8::launch_fwd<192, 128>(p, tq, tk, tv, grid, s); break;

@@ -3,4 +3,5 @@
 namespace fa8 {
 FA8_DEFINE_FWD(192, 128)
 FA8_DEFINE_FWD(192, 192)
+FA8_DEFINE_DECODE(192, 128)
 }  // namespace fa8

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa8_decode.cuh"
 #include "fa8_kernel.cuh"
 
 namespace fa8 {
@@ -15,6 +16,10 @@ cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tq, const CUtensor
 
 template <int DV>
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+
+template <int D, int DV>
+cudaError_t launch_decode(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                          const CUtensorMap &tv, dim3 grid, cudaStream_t stream);
 
 // Defines launch_fwd<D, DV>.  Dynamic shared memory above 48 KB needs an opt-in per
 // function and device; it is set on every launch (a cheap host call) so that a first
@@ -30,6 +35,21 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
                                              smem);                                          \
         if (e != cudaSuccess) return e;                                                      \
         fwd_kernel<D_, DV_><<<grid, kNumThreads, smem, stream>>>(p, tq, tk, tv);             \
+        return cudaGetLastError();                                                           \
+    }
+
+// Defines launch_decode<D, DV> (the few-rows kernel, dv a multiple of 128).
+#define FA8_DEFINE_DECODE(D_, DV_)                                                           \
+    template <>                                                                              \
+    cudaError_t launch_decode<D_, DV_>(const FwdParams &p, const CUtensorMap &tq,            \
+                                       const CUtensorMap &tk, const CUtensorMap &tv,         \
+                                       dim3 grid, cudaStream_t stream) {                     \
+        constexpr int smem = DecCfg<D_, DV_>::SMEM_BYTES;                                    \
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D_, DV_>,                         \
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,    \
+                                             smem);                                          \
+        if (e != cudaSuccess) return e;                                                      \
+        decode_kernel<D_, DV_><<<grid, kDecThreads, smem, stream>>>(p, tq, tk, tv);          \
         return cudaGetLastError();                                                           \
     }
 

@@ -60,6 +60,7 @@ SIGNATURES = {
                                               ctypes.c_void_p]),
     "fa8_check": (ctypes.c_int, [ctypes.c_void_p]),
     "fa8_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
+    "fa8_set_decode_kernel": (ctypes.c_int, [ctypes.c_int]),
     "fa8_debug_wait_probe": (ctypes.c_int, [ctypes.c_void_p]),
     "fa8_debug_set_trace_buffer": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t]),
     "fa8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -217,6 +218,11 @@ def check(stream=None) -> int:
 
 def set_wait_timeout_ns(ns: int):
     _raise(lib().fa8_set_wait_timeout_ns(int(ns)))
+
+
+def set_decode_kernel(enable: bool):
+    """Routes decode shapes (<= 16 query rows per kv-head) to the decode kernel (default)."""
+    _raise(lib().fa8_set_decode_kernel(1 if enable else 0))
 
 
 def debug_wait_probe(stream=None) -> int:

@@ -184,6 +184,15 @@ FA8_API fa8_status fa8_fwd_static_scratch(const fa8_tensor *q, const fa8_tensor 
  */
 FA8_API fa8_status fa8_check(void *stream);
 
+/*
+ * fa8_set_decode_kernel -- 1 (the default): shapes with batched q and at most 16 query rows
+ * per kv-head (Sq x Hq/Hkv <= 16, Hq/Hkv dividing 16, dv a multiple of 128) run the decode
+ * kernel, which puts the keys of a tile on the MMA's M dimension and the few query rows on
+ * N; 0: every shape runs the 128-row forward kernel.  Both compute the same attention (not
+ * bit-identically).  A process-wide setting read at each fa8_fwd call.
+ */
+FA8_API fa8_status fa8_set_decode_kernel(int enable);
+
 /* Sets the bound on every in-kernel wait (nanoseconds; default 2e9, minimum 1e5). */
 FA8_API fa8_status fa8_set_wait_timeout_ns(uint64_t ns);
 

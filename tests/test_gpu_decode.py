@@ -1,0 +1,98 @@
+"""GPU parity of the decode kernel (batched q with at most 16 query rows per kv-head: keys on
+the MMA's M dimension, query rows on N) against the fp64 oracle, and of the 128-row kernel on
+the same shapes with the decode kernel switched off."""
+import pytest
+import torch
+
+import oracle
+from fp8_attention_forward_gb300 import build, fa8, inputs
+from parity_util import assert_parity, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa8.lib()
+    yield
+    fa8.set_decode_kernel(True)
+
+
+DECODE = [
+    # (name, kwargs): every shape has Sq * (Hq / Hkv) <= 16 with Hq / Hkv dividing 16
+    ("g8_paged16_causal", dict(B=4, Hq=16, Hkv=2, D=128, DV=128, seqlens_q=[1] * 4,
+                               seqlens_k=[1, 129, 700, 2000], kv_layout="paged", page_size=16,
+                               causal=True, descale_mode="per_bkv_uniform", seed=301)),
+    ("g16_contig", dict(B=2, Hq=16, Hkv=1, D=128, DV=128, seqlens_q=[1] * 2, seqlens_k=[300] * 2,
+                        causal=False, seed=302)),
+    ("g1_mha_sq16_causal", dict(B=2, Hq=3, Hkv=3, D=128, DV=128, seqlens_q=[16] * 2,
+                                seqlens_k=[500] * 2, causal=True, seed=303)),
+    ("g4_sq4_causal_window", dict(B=3, Hq=8, Hkv=2, D=128, DV=128, seqlens_q=[4] * 3,
+                                  seqlens_k=[1000] * 3, causal=True, window_left=200, seed=304)),
+    ("g2_sq8_sink_fp16", dict(B=2, Hq=4, Hkv=2, D=128, DV=128, seqlens_q=[8] * 2,
+                              seqlens_k=[257] * 2, causal=True, sink=True, out_dtype=torch.float16,
+                              seed=305)),
+    ("g8_d192_128_varlen_kv", dict(B=3, Hq=16, Hkv=2, D=192, DV=128, seqlens_q=[1] * 3,
+                                   seqlens_k=[5, 400, 900], kv_layout="varlen", causal=True, seed=306)),
+    ("g8_d256_paged64", dict(B=2, Hq=8, Hkv=1, D=256, DV=256, seqlens_q=[1] * 2,
+                             seqlens_k=[1500, 64], kv_layout="paged", page_size=64, causal=True,
+                             descale_mode="tensor_amax", seed=307)),
+    ("g8_empty_kv", dict(B=3, Hq=8, Hkv=1, D=128, DV=128, seqlens_q=[1] * 3, seqlens_k=[0, 50, 0],
+                         kv_layout="varlen", causal=True, sink=True, seed=308)),
+]
+
+
+def _case(kw, name):
+    return inputs.make_case(name=name, **kw)
+
+
+@pytest.mark.parametrize("name,kw", DECODE, ids=[d[0] for d in DECODE])
+@pytest.mark.parametrize("decode_kernel", [True, False], ids=["decode", "rows128"])
+def test_decode_shapes(name, kw, decode_kernel):
+    case = _case(kw, name)
+    fa8.set_decode_kernel(decode_kernel)
+    try:
+        assert_parity(case)
+    finally:
+        fa8.set_decode_kernel(True)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 16])
+def test_decode_splits(splits):
+    case = _case(DECODE[0][1], "splits")
+    assert_parity(case, num_splits=splits)
+
+
+def test_decode_plan_uses_one_slot_per_request():
+    case = _case(DECODE[0][1], "plan").to("cuda")
+    s, _, grid = fa8.plan(case.q, case.k, case.v, cu_seqlens_k=case.cu_seqlens_k,
+                          block_table=case.block_table, page_size=case.page_size, num_splits=1,
+                          sm_count=152)
+    assert grid == (case.B, case.Hkv)
+
+
+@pytest.mark.parametrize("ps", [16, 128])
+def test_decode_paged_bit_exact_vs_contiguous(ps):
+    case = inputs.make_case(name="dpg", B=3, Hq=16, Hkv=2, D=128, DV=128, seqlens_q=[1] * 3,
+                            seqlens_k=[130, 1000, 555], kv_layout="paged", page_size=ps,
+                            causal=True, descale_mode="per_bkv_uniform", seed=310)
+    from test_gpu_parity import _paged_to_contig
+    contig = _paged_to_contig(case)
+    o1, l1 = run_gpu(case.to("cuda"), num_splits=1)
+    o2, l2 = run_gpu(contig.to("cuda"), num_splits=1)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+def test_decode_split_bit_exact_when_one_split_has_keys():
+    case = inputs.make_case(name="dsp", B=5, Hq=16, Hkv=2, D=128, DV=128, seqlens_q=[1] * 5,
+                            seqlens_k=[1, 17, 100, 128, 64], kv_layout="paged", page_size=16,
+                            causal=True, sink=True, descale_mode="per_bkv_uniform", seed=311)
+    c = case.to("cuda")
+    o1, l1 = run_gpu(c, num_splits=1)
+    o4, l4 = run_gpu(c, num_splits=4)
+    assert torch.equal(o1.view(torch.int16), o4.view(torch.int16))
+    assert torch.equal(l1, l4)
