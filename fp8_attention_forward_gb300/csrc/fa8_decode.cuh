@@ -88,6 +88,43 @@ __device__ __forceinline__ uint32_t swz128_offset(int q, int t) {
     return (uint32_t)(q * 128 + ((((t >> 4) ^ (q & 7))) << 4) + (t & 15));
 }
 
+// Bounded mbarrier waits whose try_wait carries a suspend-time hint: a waiting thread
+// sleeps until the phase completes (woken at once) or the hint expires, instead of
+// returning after a short fixed slice.  Same timeout and abort behaviour as Waiter.
+struct HintWaiter {
+    static constexpr uint32_t kHintNs = 100000u;
+    volatile int *abort;
+    unsigned long long timeout;
+    unsigned int *status;
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+        if (ptx::mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
+        const uint64_t t0 = ptx::globaltimer();
+        while (true) {
+            if (ptx::mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
+            if (*abort) return false;
+            if (ptx::globaltimer() - t0 > timeout) {
+                *abort = 1;
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+    __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) const {
+        const bool ok = wait(bar, parity);
+        return __all_sync(0xffffffffu, ok);
+    }
+    __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(bar, parity)) {
+            if (ptx::globaltimer() - t0 > timeout) {
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
+        }
+        return true;
+    }
+};
+
 __device__ __forceinline__ float redux_max(float v) {
     float r;
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
@@ -222,7 +259,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const Waiter W{abort_flag, p.timeout_ns, p.status};
+    const HintWaiter W{abort_flag, p.timeout_ns, p.status};
 
     if (warp == 0) {
         // ======================================================== TMA producer
@@ -411,34 +448,43 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
                 }
             }
             // tile max of every row over the 128 keys: warp reduction, then across the 4 warps
-            float *mx = mx_s + sb * kDecRows * 4;
+            const uint32_t mx_addr = ptx::smem_u32(mx_s) + (uint32_t)(sb * kDecRows * 4 * 4);
 #pragma unroll
             for (int q = 0; q < kDecRows; ++q) {
                 const float m = redux_max(u2f(u[q]));
-                if (lane == q) mx[q * 4 + sw] = m;
+                if (lane == q) ptx::st_shared_f32(mx_addr + (uint32_t)((q * 4 + sw) * 4), m);
             }
             ptx::mbar_arrive(BAR(C::B_MX + sb));
             if (!W.wait_warp(BAR(C::B_MX + sb), (uint32_t)(it >> 1) & 1u)) break;
-            // warp 4 hands this tile's rescale factors to the fold warps
-            const int as = it % C::NA;
-            if (sw == 0 && !W.wait_warp(BAR(C::B_AE + as), ((uint32_t)(it / C::NA) & 1u) ^ 1u)) break;
+            float my_alpha = 1.f;  // lane q keeps row q's rescale factor for the hand-off
 #pragma unroll
-            for (int q = 0; q < kDecRows; ++q) {
-                const float4 v = *reinterpret_cast<const float4 *>(mx + q * 4);
-                const float mt = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)) * c;
-                float alpha = 1.f;
-                if (mt > m_run[q] + kTau) {
-                    alpha = ptx::ex2(m_run[q] - mt);
-                    rsum[q] *= alpha;
-                    m_run[q] = mt;
+            for (int h8 = 0; h8 < kDecRows; h8 += 8) {
+                float4 mv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mv[i] = ptx::ld_shared_f4(mx_addr + (uint32_t)((h8 + i) * 16));
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int q = h8 + i;
+                    const float mt = fmaxf(fmaxf(mv[i].x, mv[i].y), fmaxf(mv[i].z, mv[i].w)) * c;
+                    if (mt > m_run[q] + kTau) {
+                        const float alpha = ptx::ex2(m_run[q] - mt);
+                        rsum[q] *= alpha;
+                        m_run[q] = mt;
+                        if (lane == q) my_alpha = alpha;
+                    }
                 }
-                if (sw == 0 && lane == q) alpha_s[as * kDecRows + q] = alpha;
             }
-            if (sw == 0) ptx::mbar_arrive(BAR(C::B_AF + as));
+            // warp 4 hands this tile's rescale factors to the fold warps
+            if (sw == 0) {
+                const int as = it % C::NA;
+                if (!W.wait_warp(BAR(C::B_AE + as), ((uint32_t)(it / C::NA) & 1u) ^ 1u)) break;
+                if (lane < kDecRows) ptx::st_shared_f32(ptx::smem_u32(alpha_s) + (uint32_t)((as * kDecRows + lane) * 4), my_alpha);
+                ptx::mbar_arrive(BAR(C::B_AF + as));
+            }
             // P^T(it) overwrites P^T(it - 2): wait until PV(it - 2) has read it
             if (!W.wait_warp(BAR(C::B_PE + sb), ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
-            uint8_t *phi = pbase + sb * 2 * C::P_BYTES;
-            uint8_t *plo = phi + C::P_BYTES;
+            const uint32_t phi = ptx::smem_u32(pbase) + (uint32_t)(sb * 2 * C::P_BYTES);
+            const uint32_t plo = phi + C::P_BYTES;
 #pragma unroll
             for (int q = 0; q < kDecRows; q += 2) {
                 const float b0 = kPBias - (m_run[q] == -INFINITY ? 0.f : m_run[q]);
@@ -448,14 +494,14 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
                 rsum[q] += p0;
                 rsum[q + 1] += p1;
                 const uint32_t h = ptx::cvt_e4m3x2(p1, p0);
-                phi[swz128_offset(q, t)] = (uint8_t)(h & 0xFFu);
-                phi[swz128_offset(q + 1, t)] = (uint8_t)(h >> 8);
+                ptx::st_shared_u8(phi + swz128_offset(q, t), h & 0xFFu);
+                ptx::st_shared_u8(phi + swz128_offset(q + 1, t), h >> 8);
                 if (need_mask) {  // second E4M3 term: P_lo = e4m3(p - P_hi)
                     float q0, q1;
                     ptx::e4m3x2_to_f32(h, q0, q1);
                     const uint32_t l = ptx::cvt_e4m3x2(p1 - q1, p0 - q0);
-                    plo[swz128_offset(q, t)] = (uint8_t)(l & 0xFFu);
-                    plo[swz128_offset(q + 1, t)] = (uint8_t)(l >> 8);
+                    ptx::st_shared_u8(plo + swz128_offset(q, t), l & 0xFFu);
+                    ptx::st_shared_u8(plo + swz128_offset(q + 1, t), l >> 8);
                 }
             }
             ptx::fence_proxy_async_smem();  // the PV MMA reads P^T through the async proxy
