@@ -45,7 +45,8 @@ __global__ void wait_probe_kernel(unsigned long long timeout_ns, unsigned int *s
     template <>                                                                             \
     cudaError_t launch_combine<DV_>(const CombineParams &p, cudaStream_t s) {               \
         const long long rows = (long long)p.total_q * p.Hq;                                 \
-        const unsigned blocks = (unsigned)((rows + 7) / 8);                                 \
+        const long long per_cta = 8 / p.wpr;                                                \
+        const unsigned blocks = (unsigned)((rows + per_cta - 1) / per_cta);                 \
         combine_kernel<DV_><<<blocks, 256, 0, s>>>(p);                                      \
         return cudaGetLastError();                                                          \
     }
@@ -689,6 +690,7 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
         cp.total_q = pl.total_q;
         cp.Hq = pl.Hq;
         cp.num_splits = pl.splits;
+        cp.wpr = pl.splits >= 8 ? 8 : (pl.splits >= 4 ? 4 : (pl.splits >= 2 ? 2 : 1));
         cp.q_varlen = pl.q_varlen;
         cp.Sq = pl.Sq;
         cp.o_part = p.o_part;

@@ -105,6 +105,7 @@ struct FwdParams {
 
 struct CombineParams {
     int total_q, Hq, num_splits, q_varlen, Sq;
+    int wpr;  // warps per output row (1, 2, 4 or 8): warp w % wpr takes splits s = w % wpr (mod wpr)
     const float *o_part, *lse_part;
     void *o;
     long long o_sb, o_ss, o_sh;
@@ -928,21 +929,27 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 template <int DV>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams p) {
     constexpr int PER = DV / 32;  // output columns per lane
+    __shared__ __align__(16) float part[8][DV];
+    __shared__ int part_used[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * 8 + warp;
-    if (row >= (long long)p.total_q * p.Hq) return;
-    const int tok = (int)(row / p.Hq);
-    const int hq = (int)(row % p.Hq);
-    const long long stride_s = (long long)p.total_q * p.Hq;
+    const int W = p.wpr;
+    const int sub = warp % W;
+    const long long row = (long long)blockIdx.x * (8 / W) + warp / W;
+    const long long rows = (long long)p.total_q * p.Hq;
+    const bool active = row < rows;
+    const long long stride_s = rows;
+    // every warp reads all the row's split LSEs (a few floats) for the max and the sum
     float m = -INFINITY;
-    for (int s = lane; s < p.num_splits; s += 32) m = fmaxf(m, p.lse_part[s * stride_s + row]);
+    if (active)
+        for (int s = lane; s < p.num_splits; s += 32) m = fmaxf(m, p.lse_part[s * stride_s + row]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
     float lse = -INFINITY;
-    if (m != -INFINITY) {
+    bool used = false;
+    if (active && m != -INFINITY) {
         float sw = 0.f;
         for (int s = lane; s < p.num_splits; s += 32) {
             const float l = p.lse_part[s * stride_s + row];
@@ -952,17 +959,61 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
         for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
         lse = m + ptx::lg2(sw) * kLn2;
         const float inv = 1.f / sw;
-        bool first = true;
-        for (int s = 0; s < p.num_splits; ++s) {
-            const float l = p.lse_part[s * stride_s + row];
-            if (l == -INFINITY) continue;
-            const float wgt = ptx::ex2((l - m) * kLog2e) * inv;
-            const float *src = p.o_part + (s * stride_s + row) * DV + lane * PER;
+        // this warp's splits, four loads in flight per lane
+        for (int s0 = sub; s0 < p.num_splits; s0 += 4 * W) {
+            float wgt[4];
+            float v[4][PER];
 #pragma unroll
-            for (int i = 0; i < PER; ++i) acc[i] = first ? wgt * src[i] : fmaf(wgt, src[i], acc[i]);
-            first = false;
+            for (int u = 0; u < 4; ++u) {
+                const int s = s0 + u * W;
+                const float l = s < p.num_splits ? p.lse_part[s * stride_s + row] : -INFINITY;
+                wgt[u] = l == -INFINITY ? 0.f : ptx::ex2((l - m) * kLog2e) * inv;
+                if (wgt[u] != 0.f) {
+                    const float *src = p.o_part + (s * stride_s + row) * DV + lane * PER;
+                    if constexpr (PER % 4 == 0) {
+#pragma unroll
+                        for (int i = 0; i < PER; i += 4) {
+                            const float4 x = *reinterpret_cast<const float4 *>(src + i);
+                            v[u][i] = x.x;
+                            v[u][i + 1] = x.y;
+                            v[u][i + 2] = x.z;
+                            v[u][i + 3] = x.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < PER; i += 2) {
+                            const float2 x = *reinterpret_cast<const float2 *>(src + i);
+                            v[u][i] = x.x;
+                            v[u][i + 1] = x.y;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (wgt[u] == 0.f) continue;
+#pragma unroll
+                for (int i = 0; i < PER; ++i) acc[i] = used ? fmaf(wgt[u], v[u][i], acc[i]) : wgt[u] * v[u][i];
+                used = true;
+            }
         }
     }
+    // the W warps of a row add their partial sums (only warps that had a split with keys,
+    // so that a single contributing split passes through unchanged)
+#pragma unroll
+    for (int i = 0; i < PER; ++i) part[warp][lane * PER + i] = acc[i];
+    if (lane == 0) part_used[warp] = used ? 1 : 0;
+    __syncthreads();
+    if (!active || sub != 0) return;
+    bool any = used;
+    for (int w2 = warp + 1; w2 < warp + W; ++w2) {
+        if (!part_used[w2]) continue;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[i] = any ? acc[i] + part[w2][lane * PER + i] : part[w2][lane * PER + i];
+        any = true;
+    }
+    const int tok = (int)(row / p.Hq);
+    const int hq = (int)(row % p.Hq);
     const long long beta = p.q_varlen ? 0 : tok / p.Sq;
     const long long rho = p.q_varlen ? tok : tok % p.Sq;
     if (lane == 0 && p.lse) p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
