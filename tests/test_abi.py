@@ -90,8 +90,9 @@ def test_plan_decode_splits_and_workspace(lib):
     bt = torch.zeros((B, 2048), dtype=torch.int32)
     cu = torch.zeros((B + 1,), dtype=torch.int32)
     splits, ws, grid = plan(q, kp, kp, cu_seqlens_k=cu, block_table=bt, page_size=16)
-    # 64 requests x 8 kv-heads = 512 CTAs < 8 x 152: split 3 ways
-    assert splits == 3
+    # decode kernel (8 rows per kv-head): 64 requests x 8 kv-heads = 512 CTAs < 12 x 152,
+    # split 4 ways
+    assert splits == 4
     rows = B * Hq * splits
     o_bytes = (rows * D * 4 + 255) // 256 * 256
     assert ws == o_bytes + (rows * 4 + 255) // 256 * 256
@@ -108,9 +109,25 @@ def test_plan_depends_on_sm_count_only_through_the_split_heuristic(lib):
     a = plan(q, k, v, sm=152)
     b = plan(q, k, v, sm=76)
     assert a[2][0] == b[2][0] == 1
-    assert a[0] == 64 and b[0] == 64  # capped at 64 splits
+    assert a[0] == 128 and b[0] == 128  # decode kernel: capped at 128 splits
     c = plan(*qkv(B=1, Sq=1, Sk=1024, Hq=8, Hkv=1, D=256, DV=256), sm=152)
     assert c[0] == 4  # 8 key tiles -> at most half as many splits
+
+
+def test_plan_128_row_kernel_split_cap(lib):
+    # 128-row kernel (Sq x G > 16): at most 64 splits
+    q, k, v = qkv(B=1, Sq=64, Sk=65536, Hq=8, Hkv=1, D=128, DV=128)
+    s, _, grid = plan(q, k, v, sm=152)
+    assert grid[0] == 4 and s == 64
+
+
+def test_plan_decode_rows_per_tile(lib):
+    # Sq x G <= 16 with G dividing 16: one 16-row slot per request and kv-head
+    q, k, v = qkv(B=3, Sq=2, Sk=4096, Hq=16, Hkv=2, D=128, DV=128)
+    assert plan(q, k, v, num_splits=1)[2] == (3, 2)
+    # G = 3 does not divide 16: the 128-row kernel (42 positions per tile)
+    q, k, v = qkv(B=3, Sq=2, Sk=4096, Hq=6, Hkv=2, D=128, DV=128)
+    assert plan(q, k, v, num_splits=1)[2] == (3, 2)
 
 
 def test_plan_varlen_slots(lib):
