@@ -253,8 +253,11 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
     p.P = 128 / p.G;
     p.rows_per_tile = p.P * p.G;
     // Decode shapes: batched q whose rows per kv-head (Sq x G) fit one 16-row tile.
+    // (Its launch puts the kv-heads and splits on grid x and the requests on grid y, so
+    // that the CTAs of one request, which read neighbouring bytes of the same pages, run
+    // together; grid y is limited to 65535 requests.)
     if (g_decode_kernel && q->ndim == 4 && p.DV % 128 == 0 && 16 % p.G == 0 && q->shape[1] * p.G <= 16 &&
-        q->shape[1] > 0) {
+        q->shape[1] > 0 && q->shape[0] <= 65535) {
         p.decode = 1;
         p.P = 16 / p.G;
         p.rows_per_tile = 16;
@@ -672,10 +675,11 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (pl.decode) {
+        const dim3 dgrid((unsigned)(pl.Hkv * pl.splits), (unsigned)pl.num_slots, 1);  // see make_plan
         switch (pl.D * 1000 + pl.DV) {
-            case 128128: e = fa8::launch_decode<128, 128>(p, tq, tk, tv, grid, s); break;
-            case 192128: e = fa8::launch_decode<192, 128>(p, tq, tk, tv, grid, s); break;
-            case 256256: e = fa8::launch_decode<256, 256>(p, tq, tk, tv, grid, s); break;
+            case 128128: e = fa8::launch_decode<128, 128>(p, tq, tk, tv, dgrid, s); break;
+            case 192128: e = fa8::launch_decode<192, 128>(p, tq, tk, tv, dgrid, s); break;
+            case 256256: e = fa8::launch_decode<256, 256>(p, tq, tk, tv, dgrid, s); break;
             default: return fail(FA8_ERR_UNSUPPORTED, "no decode kernel for (%d, %d)", pl.D, pl.DV);
         }
     } else switch (pl.D * 1000 + pl.DV) {

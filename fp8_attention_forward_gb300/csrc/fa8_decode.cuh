@@ -144,10 +144,12 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
     const int lane = tid & 31;
 
     // ------------------------------------------------------------ tile schedule (batched q)
-    const int b = blockIdx.x % p.B;
-    const int mb = blockIdx.x / p.B;
-    const int kvh = blockIdx.y % p.Hkv;
-    const int split = blockIdx.y / p.Hkv;
+    // grid x = kv-head + Hkv * split (fastest), grid y = request: the CTAs of one request
+    // run side by side and share the L2 lines of its pages
+    const int b = blockIdx.y % p.B;
+    const int mb = blockIdx.y / p.B;
+    const int kvh = blockIdx.x % p.Hkv;
+    const int split = blockIdx.x / p.Hkv;
     const int P = p.pos_per_tile;  // 16 / G positions
     const int q_start = b * p.Sq;
     const int Lq = p.Sq;
