@@ -51,6 +51,7 @@ __global__ void wait_probe_kernel(unsigned long long timeout_ns, unsigned int *s
         return cudaGetLastError();                                                          \
     }
 FA8_DEFINE_COMBINE(64)
+FA8_DEFINE_COMBINE(96)
 FA8_DEFINE_COMBINE(128)
 FA8_DEFINE_COMBINE(192)
 FA8_DEFINE_COMBINE(256)
@@ -176,7 +177,7 @@ fa8_status encode4(CUtensorMap *m, void *base, const uint64_t dims[4], const uin
 int chunk_of(int d) { return (d % 128 == 0) ? 128 : ((d % 64 == 0) ? 64 : 32); }
 
 bool supported_dims(int d, int dv) {
-    return (d == 64 && dv == 64) || (d == 128 && dv == 128) || (d == 192 && dv == 128) ||
+    return (d == 64 && dv == 64) || (d == 96 && dv == 96) || (d == 128 && dv == 128) || (d == 192 && dv == 128) ||
            (d == 192 && dv == 192) || (d == 256 && dv == 256);
 }
 
@@ -684,6 +685,7 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
         }
     } else switch (pl.D * 1000 + pl.DV) {
         case 64064: e = fa8::launch_fwd<64, 64>(p, tq, tk, tv, grid, s); break;
+        case 96096: e = fa8::launch_fwd<96, 96>(p, tq, tk, tv, grid, s); break;
         case 128128: e = fa8::launch_fwd<128, 128>(p, tq, tk, tv, grid, s); break;
         case 192128: e = fa8::launch_fwd<192, 128>(p, tq, tk, tv, grid, s); break;
         case 192192: e = fa8::launch_fwd<192, 192>(p, tq, tk, tv, grid, s); break;
@@ -713,6 +715,7 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
         cp.lse_ss = l_ss;
         switch (pl.DV) {
             case 64: e = fa8::launch_combine<64>(cp, s); break;
+            case 96: e = fa8::launch_combine<96>(cp, s); break;
             case 128: e = fa8::launch_combine<128>(cp, s); break;
             case 192: e = fa8::launch_combine<192>(cp, s); break;
             default: e = fa8::launch_combine<256>(cp, s); break;

@@ -1,0 +1,5 @@
+// Instantiation of the forward kernel for (d, dv) = (96, 96).
+#include "fa8_launch.h"
+namespace fa8 {
+FA8_DEFINE_FWD(96, 96)
+}  // namespace fa8

@@ -979,13 +979,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
                             v[u][i + 2] = x.z;
                             v[u][i + 3] = x.w;
                         }
-                    } else {
+                    } else if constexpr (PER % 2 == 0) {
 #pragma unroll
                         for (int i = 0; i < PER; i += 2) {
                             const float2 x = *reinterpret_cast<const float2 *>(src + i);
                             v[u][i] = x.x;
                             v[u][i + 1] = x.y;
                         }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < PER; ++i) v[u][i] = src[i];
                     }
                 }
             }
@@ -1018,17 +1021,32 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
     const long long rho = p.q_varlen ? tok : tok % p.Sq;
     if (lane == 0 && p.lse) p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
     uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + 2 * (beta * p.o_sb + rho * p.o_ss + hq * p.o_sh + lane * PER);
+    if constexpr (PER % 2 == 0) {
 #pragma unroll
-    for (int i = 0; i < PER; i += 2) {
-        uint32_t w;
-        if (p.out_fp16) {
-            __half2 h = __floats2half2_rn(acc[i], acc[i + 1]);
-            w = *reinterpret_cast<uint32_t *>(&h);
-        } else {
-            __nv_bfloat162 h = __floats2bfloat162_rn(acc[i], acc[i + 1]);
-            w = *reinterpret_cast<uint32_t *>(&h);
+        for (int i = 0; i < PER; i += 2) {
+            uint32_t w;
+            if (p.out_fp16) {
+                __half2 h = __floats2half2_rn(acc[i], acc[i + 1]);
+                w = *reinterpret_cast<uint32_t *>(&h);
+            } else {
+                __nv_bfloat162 h = __floats2bfloat162_rn(acc[i], acc[i + 1]);
+                w = *reinterpret_cast<uint32_t *>(&h);
+            }
+            *reinterpret_cast<uint32_t *>(dst + 2 * i) = w;
         }
-        *reinterpret_cast<uint32_t *>(dst + 2 * i) = w;
+    } else {  // odd columns per lane (dv = 96): one 16-bit store each
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            uint16_t w;
+            if (p.out_fp16) {
+                const __half h = __float2half_rn(acc[i]);
+                w = *reinterpret_cast<const uint16_t *>(&h);
+            } else {
+                const __nv_bfloat16 h = __float2bfloat16_rn(acc[i]);
+                w = *reinterpret_cast<const uint16_t *>(&h);
+            }
+            *reinterpret_cast<uint16_t *>(dst + 2 * i) = w;
+        }
     }
 }
 

@@ -84,7 +84,7 @@ typedef struct {
  *   out like q with DV in place of D; bf16 or fp16
  *   lse batched (B, Hq, Sq) or varlen (Hq, total_q); fp32; may be NULL
  * Q/K/V are E4M3 (E5M2 or mixed dtypes -> FA8_ERR_UNSUPPORTED).  (D, DV) is one of
- * (64,64), (128,128), (192,128), (192,192), (256,256).  Hq % Hkv == 0 and Hq/Hkv <= 128;
+ * (64,64), (96,96), (128,128), (192,128), (192,192), (256,256).  Hq % Hkv == 0 and Hq/Hkv <= 128;
  * q-head h reads kv-head h / (Hq/Hkv).  Row strides of q/k/v must be multiples of 16
  * bytes and their base pointers 16-byte aligned (they are read by TMA).
  *

@@ -37,6 +37,14 @@ def test_causal_gqa_prefill_small():
     assert_parity(inputs.causal_gqa_prefill("small"))
 
 
+@pytest.mark.parametrize("splits", [2, 5])
+def test_d96_split_combine(splits):
+    """dv = 96: three output columns per lane in the combine kernel."""
+    case = inputs.make_case(name="d96s", B=2, Hq=8, Hkv=2, D=96, DV=96, seqlens_q=[1] * 2,
+                            seqlens_k=[1500, 700], kv_layout="paged", page_size=16, causal=True, seed=117)
+    assert_parity(case, num_splits=splits)
+
+
 @pytest.mark.parametrize("splits", [0, 1, 3, 7])
 def test_paged_decode_small(splits):
     assert_parity(inputs.paged_decode("small"), num_splits=splits)
@@ -82,6 +90,15 @@ VARIANTS = [
     dict(name="varlen_empty_seqs_sink", B=3, Hq=4, Hkv=2, D=64, DV=64, seqlens_q=[5, 30, 9],
          seqlens_k=[0, 40, 3], q_layout="varlen", kv_layout="varlen", causal=True, sink=True,
          seed=113),
+]
+VARIANTS += [
+    dict(name="d96_causal_gqa", B=2, Hq=8, Hkv=2, D=96, DV=96, seqlens_q=[300] * 2, seqlens_k=[300] * 2,
+         causal=True, descale_mode="tensor_amax", seed=114),
+    dict(name="d96_decode_paged", B=3, Hq=8, Hkv=2, D=96, DV=96, seqlens_q=[1] * 3, seqlens_k=[900, 40, 2000],
+         kv_layout="paged", page_size=16, causal=True, descale_mode="per_bkv_uniform", seed=115),
+    dict(name="d96_varlen_window_sink_fp16", B=3, Hq=4, Hkv=4, D=96, DV=96, seqlens_q=[33, 200, 7],
+         seqlens_k=[33, 200, 7], q_layout="varlen", kv_layout="varlen", causal=True, window_left=50,
+         sink=True, out_dtype=torch.float16, seed=116),
 ]
 for ps in (8, 64, 128, 256):
     VARIANTS.append(dict(name=f"paged_ps{ps}", B=3, Hq=8, Hkv=2, D=128, DV=128,
