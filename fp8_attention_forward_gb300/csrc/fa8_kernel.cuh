@@ -683,48 +683,51 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     row_sum *= alpha;
                     m_run = mt;
                 }
-                const float bias = kPBias - (m_run == -INFINITY ? 0.f : m_run);
-                const uint64_t b2 = ptx::f2pack(bias, bias);
-                uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
-                // P = 2^(s c - m + 8); the packed E4M3 of keys [32q, 32q+32) goes to column
-                // 32q of the S buffer (P_lo 8 columns later on masked tiles)
+                // p = 2^(s c - m) in f16 (MUFU, two values per instruction; the argument is
+                // near 0 where p is large, so f16 keeps it to 2^-11), P = e4m3(2^8 p) with the
+                // scaling exact in f16; the row sum adds the f16 p in fp32
+                const float nm = m_run == -INFINITY ? 0.f : -m_run;
+                const uint64_t nm2 = ptx::f2pack(nm, nm);
+                constexpr uint32_t kH2Bias = 0x5C005C00u;  // f16x2 {256, 256}
+                uint64_t acc = ptx::f2pack(0.f, 0.f);
+                // the packed E4M3 of keys [32q, 32q+32) goes to column 32q of the S buffer
+                // (P_lo 8 columns later on masked tiles)
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     uint32_t w[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        float x0, x1, x2, x3;
-                        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k]), u2f(u[g][4 * k + 1])), c2, b2), x0, x1);
-                        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k + 2]), u2f(u[g][4 * k + 3])), c2, b2), x2, x3);
-                        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1), p2 = ptx::ex2(x2), p3 = ptx::ex2(x3);
-                        acc0 = ptx::fadd2(acc0, ptx::f2pack(p0, p1));
-                        acc1 = ptx::fadd2(acc1, ptx::f2pack(p2, p3));
-                        w[k] = ptx::cvt_e4m3x2(p1, p0) | (ptx::cvt_e4m3x2(p3, p2) << 16);
-                        u[g][4 * k] = __float_as_uint(p0);
-                        u[g][4 * k + 1] = __float_as_uint(p1);
-                        u[g][4 * k + 2] = __float_as_uint(p2);
-                        u[g][4 * k + 3] = __float_as_uint(p3);
+                        float y0, y1, y2, y3;
+                        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k]), u2f(u[g][4 * k + 1])), c2, nm2), y0, y1);
+                        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[g][4 * k + 2]), u2f(u[g][4 * k + 3])), c2, nm2), y2, y3);
+                        const uint32_t e01 = ptx::ex2_h2(ptx::cvt_f16x2(y1, y0));
+                        const uint32_t e23 = ptx::ex2_h2(ptx::cvt_f16x2(y3, y2));
+                        float s0, s1;
+                        ptx::h2_to_f32(ptx::hadd2(e01, e23), s0, s1);
+                        acc = ptx::fadd2(acc, ptx::f2pack(s0, s1));
+                        const uint32_t q01 = ptx::hmul2(e01, kH2Bias), q23 = ptx::hmul2(e23, kH2Bias);
+                        w[k] = ptx::cvt_e4m3x2_h2(q01) | (ptx::cvt_e4m3x2_h2(q23) << 16);
+                        u[g][2 * k] = q01;  // kept for the second term
+                        u[g][2 * k + 1] = q23;
                     }
                     ptx::tmem_st8(scol + 32 * g, w);
                     if (need_mask) {
-                        // second E4M3 term on masked tiles: P_lo = e4m3(p - P_hi)
+                        // second E4M3 term on masked tiles: P_lo = e4m3(2^8 p - P_hi), in f16
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
-                            float q0, q1, q2, q3;
-                            ptx::e4m3x2_to_f32(w[k] & 0xFFFFu, q0, q1);
-                            ptx::e4m3x2_to_f32(w[k] >> 16, q2, q3);
-                            w[k] = ptx::cvt_e4m3x2(u2f(u[g][4 * k + 1]) - q1, u2f(u[g][4 * k]) - q0) |
-                                   (ptx::cvt_e4m3x2(u2f(u[g][4 * k + 3]) - q3, u2f(u[g][4 * k + 2]) - q2) << 16);
+                            const uint32_t d01 = ptx::hsub2(u[g][2 * k], ptx::e4m3x2_to_h2(w[k] & 0xFFFFu));
+                            const uint32_t d23 = ptx::hsub2(u[g][2 * k + 1], ptx::e4m3x2_to_h2(w[k] >> 16));
+                            w[k] = ptx::cvt_e4m3x2_h2(d01) | (ptx::cvt_e4m3x2_h2(d23) << 16);
                         }
                         ptx::tmem_st8(scol + 32 * g + 8, w);
                     }
                 }
                 if (tid == 0) FA8_EV(13, it);
                 ptx::tmem_wait_st();
-                float a0, a1, a2, a3;
-                ptx::f2unpack(acc0, a0, a1);
-                ptx::f2unpack(acc1, a2, a3);
-                row_sum += (a0 + a1) + (a2 + a3);
+                float a0, a1;
+                ptx::f2unpack(acc, a0, a1);
+                // the f16 p carry no 2^8 factor: scale the tile's sum to the biased row sum
+                row_sum += (a0 + a1) * 256.f;
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(BAR(C::B_PF + sb));

@@ -286,5 +286,52 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint32_t pair, float &lo, float &h
     hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
 }
 
+// ---------------------------------------------------------------- packed f16 pairs
+// {hi, lo} -> f16x2 (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t cvt_f16x2(float hi, float lo) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// 2^x on both halves (MUFU, one instruction for two values)
+__device__ __forceinline__ uint32_t ex2_h2(uint32_t x) {
+    uint32_t d;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(d) : "r"(x));
+    return d;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// f16x2 -> E4M3 pair (16 bits: lo value in the low byte), round to nearest even, saturating
+__device__ __forceinline__ uint32_t cvt_e4m3x2_h2(uint32_t h2) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+    return static_cast<uint32_t>(r);
+}
+// E4M3 pair (low 16 bits) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t pair) {
+    uint32_t h2;
+    const uint16_t b = static_cast<uint16_t>(pair);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(b));
+    return h2;
+}
+// f16x2 -> (lo, hi) floats, exact
+__device__ __forceinline__ void h2_to_f32(uint32_t h2, float &lo, float &hi) {
+    lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+    hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+
 }  // namespace ptx
 }  // namespace fa8
