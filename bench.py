@@ -38,10 +38,10 @@ METRIC = "FP8 attn fwd TFLOP/s (prefill) & decode HBM GB/s; % of GB300 roofline"
 # DRAM bytes (read + write) per launch from one ncu capture of each timed kernel (summaries
 # under profiles/), valid only while the kernel sources hash to the value recorded with it.
 PROFILED_TRAFFIC = {
-    "prefill": {"kernel": "fwd_kernel<128,128>", "bytes": 68.98e6,
-                "sources": ["fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "d44996a6b8dfa04b"},
-    "decode": {"kernel": "decode_kernel<128,128>", "bytes": 2395.7e6,
-               "sources": ["fa8_decode.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "31208840f294d199"},
+    "prefill": {"kernel": "fwd_kernel<128,128>", "bytes": 68.74e6,
+                "sources": ["fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "e5add3c4e08e6c32"},
+    "decode": {"kernel": "decode_kernel<128,128>", "bytes": 2078.6e6,
+               "sources": ["fa8_decode.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "4765a9e017eb9823"},
 }
 
 
