@@ -328,9 +328,9 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
     const int max_tiles = (int)std::max(1LL, (p.max_lk + 127) / 128);
     int splits;
     if (num_splits == 0) {
-        // enough CTAs to fill the SMs several times over (the decode kernel runs two per SM
-        // and is cheaper per CTA, so it is given more), never fewer than two tiles a split
-        const long long target = (p.decode ? 12LL : 8LL) * sm_count;
+        // enough CTAs to fill the SMs several times over, never fewer than two tiles a split
+        // (the decode kernel, cheaper per CTA, may split up to 128 ways)
+        const long long target = 8LL * sm_count;
         const long long cap = p.decode ? 128 : 64;
         if (base_ctas >= target || max_tiles < 4) {
             splits = 1;

@@ -90,9 +90,9 @@ def test_plan_decode_splits_and_workspace(lib):
     bt = torch.zeros((B, 2048), dtype=torch.int32)
     cu = torch.zeros((B + 1,), dtype=torch.int32)
     splits, ws, grid = plan(q, kp, kp, cu_seqlens_k=cu, block_table=bt, page_size=16)
-    # decode kernel (8 rows per kv-head): 64 requests x 8 kv-heads = 512 CTAs < 12 x 152,
-    # split 4 ways
-    assert splits == 4
+    # decode kernel (8 rows per kv-head): 64 requests x 8 kv-heads = 512 CTAs < 8 x 152,
+    # split 3 ways
+    assert splits == 3
     rows = B * Hq * splits
     o_bytes = (rows * D * 4 + 255) // 256 * 256
     assert ws == o_bytes + (rows * 4 + 255) // 256 * 256

@@ -246,3 +246,35 @@ def test_wait_timeout_is_reported():
         fa8.set_wait_timeout_ns(2_000_000_000)
     # the context is still usable afterwards
     assert_parity(inputs.tiny_dense())
+
+
+# ------------------------------------------------------------------ CUDA graph capture
+@pytest.mark.parametrize("make,splits", [(lambda: inputs.causal_gqa_prefill("small"), 0),
+                                         (lambda: inputs.paged_decode("small"), 3)],
+                         ids=["prefill", "decode_split3"])
+def test_graph_capture_replay_matches_direct(make, splits):
+    """Launch choices depend only on shapes, so a call captured in a CUDA graph replays to
+    the same bits as a direct call (workspace, outputs and inputs at fixed addresses)."""
+    c = make().to("cuda")
+    s, nbytes, _ = fa8.plan(c.q, c.k, c.v, cu_seqlens_q=c.cu_seqlens_q, cu_seqlens_k=c.cu_seqlens_k,
+                            block_table=c.block_table, page_size=c.page_size, num_splits=splits)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    out_d, lse_d = run_gpu(c, num_splits=splits, workspace=ws)
+    out = torch.empty_like(out_d)
+    lse = torch.empty_like(lse_d)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        fa8.fwd_case(c, out=out, lse=lse, workspace=ws, num_splits=splits)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    out.zero_()
+    lse.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa8.fwd_case(c, out=out, lse=lse, workspace=ws, num_splits=splits)
+    g.replay()
+    torch.cuda.synchronize()
+    assert fa8.check() == fa8.FA8_SUCCESS
+    assert torch.equal(out.view(torch.int16), out_d.view(torch.int16))
+    assert torch.equal(lse, lse_d)
