@@ -11,8 +11,10 @@ Timing: W untimed steps, then K steps; before every step a 256 MB buffer is writ
 flush L2 (129 MB); each step's forward call is bracketed by CUDA events on the launching
 stream; ms_per_step is the mean over the K steps, max over ranks.  `e2e` repeats the
 measurement through the public call with the inputs copied from pinned host memory and
-the output copied back inside the timed region.  `--impl reference` times the fp64 CPU
-oracle (the only reference this path has) on a bounded sample of the same workload.
+the output copied back inside the timed region (pipelined over two buffer sets so that the
+copies of neighbouring steps overlap the forward; the serial time is reported beside it).
+`--impl reference` times the fp64 CPU oracle (the only reference this path has) on a
+bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -174,41 +176,88 @@ def bench_case(case, steps, warmup, flush, fa8, num_splits=0):
 
 
 def bench_e2e(case, steps, warmup, flush, fa8, num_splits=0):
-    """Per step: pinned host -> device copies of Q/K/V (and the small index tensors), the
-    forward, and the output/LSE copied back to pinned host memory."""
-    dev = case
+    """End-to-end through the public call: every step copies its inputs (Q/K/V and the small
+    index tensors) from pinned host memory, runs the forward and copies O and LSE back to
+    pinned host memory.  Two buffer sets and three streams let the copies of neighbouring
+    steps overlap the forward of the current one (H2D of step i+1 and D2H of step i-1 run
+    while step i computes), as a serving loop would; every step's copies are inside the
+    timed region, which runs from the first H2D to the last D2H.  The L2 flush is issued on
+    the compute stream before every forward.  Returns the pipelined and the serial time per
+    step."""
+    import dataclasses
+
     host = {}
     names = ["q", "k", "v", "descale_q", "descale_k", "descale_v", "cu_seqlens_q", "cu_seqlens_k",
              "block_table", "sink"]
     for n in names:
-        t = getattr(dev, n)
+        t = getattr(case, n)
         if t is not None:
             host[n] = t.cpu().pin_memory()
-    dst = {n: torch.empty_like(getattr(dev, n)) for n in host}
-    import dataclasses
-
-    dcase = dataclasses.replace(dev, **dst)
-    splits, ws_bytes, _ = fa8.plan(dcase.q, dcase.k, dcase.v, cu_seqlens_q=dcase.cu_seqlens_q,
-                                   cu_seqlens_k=dcase.cu_seqlens_k, block_table=dcase.block_table,
-                                   page_size=dcase.page_size, num_splits=num_splits)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
-    out = torch.empty(tuple(dcase.q.shape[:-1]) + (dcase.DV,), dtype=dcase.out_dtype, device="cuda")
-    lse = (torch.empty((dcase.q.shape[0], dcase.Hq, dcase.q.shape[1]), dtype=torch.float32, device="cuda")
-           if dcase.q.dim() == 4 else torch.empty((dcase.Hq, dcase.q.shape[0]), dtype=torch.float32, device="cuda"))
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    sets = []
+    for _ in range(2):
+        dst = {n: torch.empty_like(getattr(case, n)) for n in host}
+        dcase = dataclasses.replace(case, **dst)
+        out = torch.empty(tuple(dcase.q.shape[:-1]) + (dcase.DV,), dtype=dcase.out_dtype, device="cuda")
+        lse = (torch.empty((dcase.q.shape[0], dcase.Hq, dcase.q.shape[1]), dtype=torch.float32, device="cuda")
+               if dcase.q.dim() == 4 else torch.empty((dcase.Hq, dcase.q.shape[0]), dtype=torch.float32, device="cuda"))
+        sets.append({"dst": dst, "case": dcase, "out": out, "lse": lse,
+                     "out_h": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                     "lse_h": torch.empty(lse.shape, dtype=lse.dtype).pin_memory()})
+    c0 = sets[0]["case"]
+    splits, ws_bytes, _ = fa8.plan(c0.q, c0.k, c0.v, cu_seqlens_q=c0.cu_seqlens_q, cu_seqlens_k=c0.cu_seqlens_k,
+                                   block_table=c0.block_table, page_size=c0.page_size, num_splits=num_splits)
+    ws = [torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+    d2h = sets[0]["out"].numel() * sets[0]["out"].element_size() + sets[0]["lse"].numel() * sets[0]["lse"].element_size()
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
-    def run():
-        for n, t in host.items():
-            dst[n].copy_(t, non_blocking=True)
-        fa8.fwd_case(dcase, out=out, lse=lse, workspace=ws, num_splits=num_splits)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+    def pipelined(n):
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_cmp = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(s_in)
+        for i in range(n):
+            S = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_cmp[i - 2])  # inputs of set i%2 consumed by step i-2
+                for k_, t in host.items():
+                    S["dst"][k_].copy_(t, non_blocking=True)
+                ev_in[i].record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(ev_in[i])
+                if i >= 2:
+                    s_cmp.wait_event(ev_out[i - 2])  # outputs of set i%2 read back by step i-2
+                flush.fill_(1)
+                fa8.fwd_case(S["case"], out=S["out"], lse=S["lse"], workspace=ws[i % 2], num_splits=num_splits,
+                             stream=s_cmp)
+                ev_cmp[i].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[i])
+                S["out_h"].copy_(S["out"], non_blocking=True)
+                S["lse_h"].copy_(S["lse"], non_blocking=True)
+                ev_out[i].record(s_out)
+        t1.record(s_out)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / n
 
-    times = time_kernel(run, steps, warmup, flush)
-    return {"ms": statistics.mean(times), "h2d": h2d, "d2h": d2h}
+    def serial():
+        S = sets[0]
+        for k_, t in host.items():
+            S["dst"][k_].copy_(t, non_blocking=True)
+        fa8.fwd_case(S["case"], out=S["out"], lse=S["lse"], workspace=ws[0], num_splits=num_splits)
+        S["out_h"].copy_(S["out"], non_blocking=True)
+        S["lse_h"].copy_(S["lse"], non_blocking=True)
+
+    pipelined(max(warmup, 3))
+    ms = pipelined(steps)
+    ser = statistics.mean(time_kernel(serial, max(3, steps // 2), 3, flush))
+    st = fa8.check()
+    if st != fa8.FA8_SUCCESS:
+        raise RuntimeError(f"device status {st}")
+    return {"ms": ms, "ms_serial": ser, "h2d": h2d, "d2h": d2h}
 
 
 def cpu_oracle_sample(case, budget_s=15.0, seed=0):
@@ -311,7 +360,7 @@ def main():
     tflops_rank = flops / (ms * 1e-3) / 1e12
     value = tflops_rank * world
 
-    e2e = bench_e2e(prefill, max(3, args.steps // 2), 3, flush, fa8)
+    e2e = bench_e2e(prefill, max(4, args.steps), max(3, args.warmup), flush, fa8)
     e2e_ms = _max_over_ranks(e2e["ms"], world)
 
     decode = None
@@ -352,7 +401,9 @@ def main():
                          "kernel": PROFILED_TRAFFIC["prefill"]["kernel"],
                          "peak_source": f"{peaks['source']} bf16 burst x2 (dense FP8 = 2x bf16)"},
             "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e_ms},
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e_ms,
+                    "mode": "pipelined: 2 buffer sets, copy-in / compute / copy-out streams",
+                    "ms_per_step_serial": e2e["ms_serial"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
             "clocks": clk, "decode": decode, "cpu_baseline": cpu, "wall_s_timed_region": wall,
         }
