@@ -15,8 +15,10 @@
 // instead of spending a 128-row softmax on a handful of rows.  P^T is written to shared
 // memory (K-major, 128-byte swizzle) with plain stores and read by the PV MMA from there.
 //
-// Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 4-7 softmax (thread
-// = key of the tile), warps 8-11 fold and epilogue (thread = row of O^T, i.e. a dv index).
+// Roles (384 threads): warp 0 TMA producer, warp 1 issues the QK MMAs and warp 2 the PV
+// MMAs (two issuers, so that neither waits behind the other's barriers), warps 4-7 softmax
+// (thread = key of the tile), warps 8-11 fold and epilogue (thread = row of O^T, i.e. a dv
+// index).
 #pragma once
 
 #include "fa8_kernel.cuh"
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         ptx::mbar_init(BAR(C::B_MX + 1), 128);
         ptx::mbar_init(BAR(C::B_SUM), 128);
         ptx::mbar_init(BAR(C::B_FIN), 32);
-        ptx::mbar_init(BAR(C::B_DONE), 1);
+        ptx::mbar_init(BAR(C::B_DONE), 2);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -334,8 +336,9 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
                 W.drain(BAR(C::B_VF + i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ======================================================== MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ======================================================== MMA issuers: warp 1 issues
+        // S^T = K Q^T, warp 2 issues O^T = V^T P^T; each commits its own barriers
         constexpr uint32_t kIdescS = idesc_e4m3(kTileN, kDecRows, false);
         constexpr uint32_t kIdescO = idesc_e4m3(128, kDecRows, false) | (1u << 15);  // A (V) MN-major
         const uint64_t da0 = sdesc(sK, 16, 8 * C::CW, swz_layout(C::CW));
@@ -396,20 +399,22 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
             __syncwarp();
             return true;
         };
-        // S(j + 2) reuses the S^T buffer of S(j) once the softmax has read it; P has its own
-        // buffers, so QK(j + 2) is issued before PV(j)
-        if (ok && n_tiles > 0) ok = do_qk(0);
-        if (ok && n_tiles > 1) ok = do_qk(1);
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            if (j + 2 < n_tiles) {
+        // S(j + 2) reuses the S^T buffer of S(j) once the softmax has read it (P has its own
+        // buffers), so the QK issuer runs two tiles ahead; the PV issuer follows the softmax
+        if (warp == 1) {
+            if (ok && n_tiles > 0) ok = do_qk(0);
+            if (ok && n_tiles > 1) ok = do_qk(1);
+            for (int j = 0; ok && j + 2 < n_tiles; ++j) {
                 ok = W.wait_warp(BAR(C::B_SE + (j & 1)), (uint32_t)(j >> 1) & 1u);
                 if (ok) ok = do_qk(j + 2);
             }
-            if (ok) ok = do_pv(j);
+        } else {
+            for (int j = 0; ok && j < n_tiles; ++j) ok = do_pv(j);
         }
+        // both issuers' MMAs must finish before TMEM is released (B_DONE counts two commits)
         if (leader) ptx::tc_commit(BAR(C::B_DONE));
         __syncwarp();
-        W.drain(BAR(C::B_DONE), 0);
+        if (warp == 1) W.drain(BAR(C::B_DONE), 0);
         __syncwarp();
     } else if (warp >= 4 && warp < 8) {
         // ======================================================== softmax (thread = key t)

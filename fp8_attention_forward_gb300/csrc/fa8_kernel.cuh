@@ -44,9 +44,11 @@ constexpr int kTileM = 128;     // Q rows per CTA = TMEM lanes
 constexpr int kTileN = 128;     // keys per KV tile
 constexpr int kNumThreads = 512;
 // registers per thread after setmaxnreg; 256 x 112 + 128 x 240 + 128 x 48 = 512 x 128 (launch)
+constexpr int kLaunchRegs = 128;
 constexpr int kRegsSoft = 112;
 constexpr int kRegsCorr = 240;
 constexpr int kRegsCtl = 48;
+static_assert(2 * kRegsSoft + kRegsCorr + kRegsCtl == 4 * kLaunchRegs, "register split");
 constexpr float kTau = 0.75f;   // lazy-rescale threshold, log2 units
 constexpr float kPBias = 8.0f;  // P carries a factor 2^8
 constexpr float kLog2e = 1.4426950408889634f;
