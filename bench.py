@@ -295,6 +295,38 @@ def cpu_oracle_sample(case, budget_s=15.0, seed=0):
     return total_flops / dt, rows_done, dt
 
 
+def _decode_kernel_name(case):
+    """The kernel include/fa8.h documents for this shape: the few-rows decode kernel when
+    query positions x (Hq / Hkv) <= 16 with Hq / Hkv dividing 16 (batched q, dv % 128 = 0)."""
+    g = case.Hq // case.Hkv
+    sq = case.seqlens_q[0]
+    few = case.q_layout == "batched" and case.DV % 128 == 0 and 16 % g == 0 and sq * g <= 16
+    return f"decode_kernel<{case.D},{case.DV}>" if few else f"fwd_kernel<{case.D},{case.DV}>"
+
+
+def decode_steps_suite(args):
+    """Times every inputs.DECODE_STEP_SHAPES case (default split heuristic, L2 flushed before
+    every step) and prints one JSON line per shape."""
+    import torch
+
+    from fp8_attention_forward_gb300 import fa8
+
+    peaks = _peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for shape in inputs.DECODE_STEP_SHAPES:
+        case = inputs.decode_step(shape, device="cuda")
+        r = bench_case(case, args.steps, args.warmup, flush, fa8)
+        nb = inputs.algorithmic_bytes(case)
+        gbs = nb / (r["ms"] * 1e-3) / 1e9
+        print(json.dumps({"suite": "decode-steps", "shape": shape[0], "us": r["ms"] * 1e3,
+                          "us_min": r["ms_min"] * 1e3, "splits": r["splits"],
+                          "kernel": _decode_kernel_name(case),
+                          "algorithmic_bytes": nb, "GB/s": gbs,
+                          "frac_hbm": gbs / peaks["hbm_gbs"], "steps": args.steps,
+                          "warmup": args.warmup, "l2": "256 MB buffer written before every step"}))
+        del case, r
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -303,7 +335,12 @@ def main():
     ap.add_argument("--impl", default="fa8", choices=["fa8", "reference"])
     ap.add_argument("--no-decode", action="store_true", help="skip the paged-decode figure")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--suite", default="", choices=["", "decode-steps"],
+                    help="decode-steps: one JSON line per served-model decode step shape "
+                         "(kernel time incl. the split combine) instead of the headline line")
     args = ap.parse_args()
+    if args.suite == "decode-steps":
+        return decode_steps_suite(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

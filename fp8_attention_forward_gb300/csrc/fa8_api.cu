@@ -702,6 +702,14 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
         cp.wpr = pl.splits >= 8 ? 8 : (pl.splits >= 4 ? 4 : (pl.splits >= 2 ? 2 : 1));
         cp.q_varlen = pl.q_varlen;
         cp.Sq = pl.Sq;
+        cp.B = p.B;
+        cp.pos_per_tile = p.pos_per_tile;
+        cp.kv_mode = p.kv_mode;
+        cp.Sk = p.Sk;
+        cp.causal = p.causal;
+        cp.window_left = p.window_left;
+        cp.cu_q = p.cu_q;
+        cp.cu_k = p.cu_k;
         cp.o_part = p.o_part;
         cp.lse_part = p.lse_part;
         cp.o = p.o;

@@ -173,16 +173,9 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
     if (pos0 >= Lq) return;
     const int pos_last = min(pos0 + P, Lq) - 1;
     const int delta = Lk - Lq;
-    const int kv_end = p.causal ? min(Lk, pos_last + delta + 1) : Lk;
-    const int kv_beg = p.window_left >= 0 ? max(0, pos0 + delta - p.window_left) : 0;
-    int t_beg = 0, n_tiles = 0;
-    if (kv_end > kv_beg) {
-        const int tb = kv_beg / kTileN;
-        const int te = (kv_end + kTileN - 1) / kTileN;
-        const int per = (te - tb + p.num_splits - 1) / p.num_splits;
-        t_beg = tb + split * per;
-        n_tiles = max(0, min(te, t_beg + per) - t_beg);
-    }
+    const SplitRange sr = split_range(Lq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits, split);
+    if (split >= sr.eff) return;  // this tile runs fewer splits; the combine skips this one
+    const int t_beg = sr.t_beg, n_tiles = sr.n_tiles;
     const bool has_sink = p.sink != nullptr && (!p.split_mode || split == 0);
     // row q of the tile: position pos0 + q / G, q-head kvh * G + q % G
     auto row_pos = [&](int q) { return pos0 + q / p.G; };

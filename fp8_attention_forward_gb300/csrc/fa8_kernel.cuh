@@ -107,6 +107,9 @@ struct FwdParams {
 
 struct CombineParams {
     int total_q, Hq, num_splits, q_varlen, Sq;
+    // what the forward kernels derive each row's split count from (see split_range)
+    int B, pos_per_tile, kv_mode, Sk, causal, window_left;
+    const int *cu_q, *cu_k;
     int wpr;  // warps per output row (1, 2, 4 or 8): warp w % wpr takes splits s = w % wpr (mod wpr)
     const float *o_part, *lse_part;
     void *o;
@@ -253,6 +256,36 @@ __device__ __forceinline__ bool tile_needs_mask(int k0, int Lk, int causal, int 
            (window_left >= 0 && k0 < pos_last + delta - window_left);
 }
 
+// Splits of a tile's key range (graph-safe: the launch fixes an upper bound, the device
+// picks the count per tile).  The visible keys of query positions [pos0, pos_last] span KV
+// tiles [tb, te); the tile uses eff = clamp(ceil((te - tb) / kMinTilesPerSplit), 1,
+// num_splits) splits of ceil((te - tb) / eff) tiles each, so a request whose keys are much
+// fewer than the launch was sized for (a block table as wide as the longest request) runs
+// few splits of a useful length instead of many empty or one-tile ones.  Splits >= eff do
+// nothing and the combine kernel, which evaluates the same function per row, never reads
+// them; split 0 always runs (it also writes the result of a tile without visible keys).
+constexpr int kMinTilesPerSplit = 2;
+struct SplitRange {
+    int t_beg, n_tiles, eff;
+};
+__device__ __forceinline__ SplitRange split_range(int Lq, int Lk, int pos0, int pos_last, int causal,
+                                                  int window_left, int num_splits, int split) {
+    const int delta = Lk - Lq;
+    const int kv_end = causal ? min(Lk, pos_last + delta + 1) : Lk;
+    const int kv_beg = window_left >= 0 ? max(0, pos0 + delta - window_left) : 0;
+    SplitRange r{0, 0, 1};
+    if (kv_end > kv_beg) {
+        const int tb = kv_beg / kTileN;
+        const int te = (kv_end + kTileN - 1) / kTileN;
+        const int nt = te - tb;
+        r.eff = max(1, min(num_splits, (nt + kMinTilesPerSplit - 1) / kMinTilesPerSplit));
+        const int per = (nt + r.eff - 1) / r.eff;
+        r.t_beg = tb + split * per;
+        r.n_tiles = max(0, min(te, r.t_beg + per) - r.t_beg);
+    }
+    return r;
+}
+
 // Maps a varlen grid slot to (request, slot within the request): the slots enumerate each
 // request's groups of `per_slot` consecutive m-blocks in order; within a request the order
 // is reversed so that, with a causal mask, the longer rows start first.  Whole warp must
@@ -356,16 +389,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (pos0 >= Lq) return;
     const int pos_last = min(pos0 + P, Lq) - 1;
     const int delta = Lk - Lq;
-    const int kv_end = p.causal ? min(Lk, pos_last + delta + 1) : Lk;
-    const int kv_beg = p.window_left >= 0 ? max(0, pos0 + delta - p.window_left) : 0;
-    int t_beg = 0, n_tiles = 0;
-    if (kv_end > kv_beg) {
-        const int tb = kv_beg / kTileN;
-        const int te = (kv_end + kTileN - 1) / kTileN;
-        const int per = (te - tb + p.num_splits - 1) / p.num_splits;
-        t_beg = tb + split * per;
-        n_tiles = max(0, min(te, t_beg + per) - t_beg);
-    }
+    const SplitRange sr = split_range(Lq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits, split);
+    if (split >= sr.eff) return;  // this tile runs fewer splits; the combine skips this one
+    const int t_beg = sr.t_beg, n_tiles = sr.n_tiles;
 
     // ------------------------------------------------------------ per-row facts
     const int r = tid & 127;  // tile row of softmax / correction threads
@@ -943,10 +969,35 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
     const long long rows = (long long)p.total_q * p.Hq;
     const bool active = row < rows;
     const long long stride_s = rows;
+    const int tok = (int)(row / p.Hq);
+    const int hq = (int)(row % p.Hq);
+    // the splits the forward ran for this row's tile (split_range on the same inputs)
+    int ns = 1;
+    if (active) {
+        int b = 0, pos = tok, Lq = p.Sq;
+        if (p.q_varlen) {
+            int lo = 0, hi = p.B - 1;  // last request whose first token is <= tok
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (p.cu_q[mid] <= tok) lo = mid;
+                else hi = mid - 1;
+            }
+            b = lo;
+            pos = tok - p.cu_q[b];
+            Lq = p.cu_q[b + 1] - p.cu_q[b];
+        } else {
+            b = tok / p.Sq;
+            pos = tok - b * p.Sq;
+        }
+        const int Lk = p.kv_mode == 0 ? p.Sk : p.cu_k[b + 1] - p.cu_k[b];
+        const int pos0 = pos / p.pos_per_tile * p.pos_per_tile;
+        const int pos_last = min(pos0 + p.pos_per_tile, Lq) - 1;
+        ns = split_range(Lq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits, 0).eff;
+    }
     // every warp reads all the row's split LSEs (a few floats) for the max and the sum
     float m = -INFINITY;
     if (active)
-        for (int s = lane; s < p.num_splits; s += 32) m = fmaxf(m, p.lse_part[s * stride_s + row]);
+        for (int s = lane; s < ns; s += 32) m = fmaxf(m, p.lse_part[s * stride_s + row]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float acc[PER];
@@ -956,7 +1007,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
     bool used = false;
     if (active && m != -INFINITY) {
         float sw = 0.f;
-        for (int s = lane; s < p.num_splits; s += 32) {
+        for (int s = lane; s < ns; s += 32) {
             const float l = p.lse_part[s * stride_s + row];
             if (l != -INFINITY) sw += ptx::ex2((l - m) * kLog2e);
         }
@@ -965,13 +1016,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
         lse = m + ptx::lg2(sw) * kLn2;
         const float inv = 1.f / sw;
         // this warp's splits, four loads in flight per lane
-        for (int s0 = sub; s0 < p.num_splits; s0 += 4 * W) {
+        for (int s0 = sub; s0 < ns; s0 += 4 * W) {
             float wgt[4];
             float v[4][PER];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int s = s0 + u * W;
-                const float l = s < p.num_splits ? p.lse_part[s * stride_s + row] : -INFINITY;
+                const float l = s < ns ? p.lse_part[s * stride_s + row] : -INFINITY;
                 wgt[u] = l == -INFINITY ? 0.f : ptx::ex2((l - m) * kLog2e) * inv;
                 if (wgt[u] != 0.f) {
                     const float *src = p.o_part + (s * stride_s + row) * DV + lane * PER;
@@ -1020,8 +1071,6 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
         for (int i = 0; i < PER; ++i) acc[i] = any ? acc[i] + part[w2][lane * PER + i] : part[w2][lane * PER + i];
         any = true;
     }
-    const int tok = (int)(row / p.Hq);
-    const int hq = (int)(row % p.Hq);
     const long long beta = p.q_varlen ? 0 : tok / p.Sq;
     const long long rho = p.q_varlen ? tok : tok % p.Sq;
     if (lane == 0 && p.lse) p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;

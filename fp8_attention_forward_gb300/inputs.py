@@ -358,6 +358,36 @@ def varlen_swa_prefill(scale="full", device="cpu") -> Case:
                      out_dtype=torch.float16, seed=4, device=device)
 
 
+# Per-layer decode steps of served models ("[Cute,Fwd,Sm90] Native FP8 (E4M3 Q/K/V) forward
+# for Hopper", Performance: requests x query tokens at a context length, 16-token pages,
+# causal, with the split-KV combine).  The head counts per GPU are those of the public model
+# configurations under the stated tensor parallelism; the d=256 windowed rows of that table
+# are left out because the page does not give their head counts.  One more row runs the
+# four-token shape with 64-token pages.
+DECODE_STEP_SHAPES = [
+    # (name, requests, query tokens, context, Hq, Hkv, page size)
+    ("llama3.1-8b-tp1 1x1 4k", 1, 1, 4096, 32, 8, 16),
+    ("llama3.1-8b-tp1 32x1 2k", 32, 1, 2048, 32, 8, 16),
+    ("llama3.1-8b-tp1 128x1 1k", 128, 1, 1024, 32, 8, 16),
+    ("llama3.1-8b-tp1 16x1 16k", 16, 1, 16384, 32, 8, 16),
+    ("llama3.1-8b-tp1 32x4 4k", 32, 4, 4096, 32, 8, 16),
+    ("llama3.1-70b-tp4 64x1 4k", 64, 1, 4096, 16, 2, 16),
+    ("llama3.1-70b-tp4 8x1 32k", 8, 1, 32768, 16, 2, 16),
+    ("qwen3-32b-tp2 32x1 8k", 32, 1, 8192, 32, 4, 16),
+    ("llama3.1-8b-tp1 32x4 4k page64", 32, 4, 4096, 32, 8, 64),
+]
+
+
+def decode_step(shape, device="cpu", max_seqlen_k=32768) -> Case:
+    """One of DECODE_STEP_SHAPES: e4m3(N(0,1)) Q/K/V, per-(batch, kv-head) descales, d=128,
+    every request at the stated context, block tables as wide as max_seqlen_k."""
+    name, reqs, sq, ctx, hq, hkv, ps = shape
+    return make_case(name=name, B=reqs, Hq=hq, Hkv=hkv, D=128, DV=128, seqlens_q=[sq] * reqs,
+                     seqlens_k=[ctx] * reqs, q_layout="batched", kv_layout="paged", page_size=ps,
+                     table_width=max_seqlen_k // ps, causal=True, descale_mode="per_bkv_uniform",
+                     out_dtype=torch.bfloat16, seed=5, device=device)
+
+
 def algorithmic_flops(case: Case) -> float:
     """2*(d+dv) flops per unmasked (row, key) pair, summed over heads."""
     return 2.0 * (case.D + case.DV) * case.pairs()

@@ -102,9 +102,12 @@ typedef struct {
  * causal: 0/1, bottom-right aligned (key j visible to query i when j <= i + Lk - Lq).
  * window_left: -1 = unbounded, else keys j >= i + Lk - Lq - window_left stay visible.
  * softmax_scale: <= 0 selects 1/sqrt(D).
- * num_splits: 0 = heuristic, 1 = no split, n > 1 = split each request's key range in
- *   n parts and merge them with a second kernel.  The choice depends only on shapes and
- *   the device's SM count, never on device values, so a call can be graph-captured.
+ * num_splits: 0 = heuristic, 1 = no split, n > 1 = launch n splits of each tile's key
+ *   range and merge them with a second kernel.  The launch depends only on shapes and the
+ *   device's SM count, never on device values, so a call can be graph-captured.  On the
+ *   device, a tile whose visible keys span t KV tiles of 128 keys runs
+ *   min(n, max(1, ceil(t / 2))) of the launched splits (at least two KV tiles per split);
+ *   the other splits exit at once and the merge does not read them.
  * workspace / workspace_bytes: device scratch for the split partials, at least
  *   fa8_fwd_workspace_size() bytes (may be NULL/0 when that size is 0).
  */

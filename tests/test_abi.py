@@ -9,7 +9,7 @@ import subprocess
 import pytest
 import torch
 
-from fp8_attention_forward_gb300 import build, fa8
+from fp8_attention_forward_gb300 import build, fa8, inputs
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "fa8.h")
@@ -200,3 +200,17 @@ def test_forward_validates_before_touching_the_device(lib):
     out = torch.zeros((1, 8, 2, 128), dtype=torch.float32)
     with pytest.raises(fa8.Fa8Error, match="bf16 or fp16"):
         fa8.fwd(q, k, v, out=out, workspace=torch.zeros(16, dtype=torch.uint8))
+
+
+def test_decode_step_shapes_use_the_decode_kernel(lib):
+    # every served-model decode step shape has <= 16 rows per kv-head: one decode-kernel slot
+    # per request and kv-head, whatever the block table width (zero tensors of the shapes)
+    for name, reqs, sq, ctx, hq, hkv, ps in inputs.DECODE_STEP_SHAPES:
+        g = hq // hkv
+        assert 16 % g == 0 and sq * g <= 16, name
+        q = torch.zeros((reqs, sq, hq, 128), dtype=torch.uint8).view(E4M3)
+        kp = torch.zeros((reqs * ctx // ps, ps, hkv, 128), dtype=torch.uint8).view(E4M3)
+        bt = torch.zeros((reqs, 32768 // ps), dtype=torch.int32)
+        cu = torch.zeros((reqs + 1,), dtype=torch.int32)
+        s, _, grid = plan(q, kp, kp, cu_seqlens_k=cu, block_table=bt, page_size=ps, num_splits=1)
+        assert s == 1 and grid == (reqs, hkv), name

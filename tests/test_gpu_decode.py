@@ -42,6 +42,11 @@ DECODE = [
                              descale_mode="tensor_amax", seed=307)),
     ("g8_empty_kv", dict(B=3, Hq=8, Hkv=1, D=128, DV=128, seqlens_q=[1] * 3, seqlens_k=[0, 50, 0],
                          kv_layout="varlen", causal=True, sink=True, seed=308)),
+    # four query tokens per request, GQA 32/8, 64-token pages in a table as wide as 32k keys
+    ("g4_sq4_paged64_wide_table", dict(B=3, Hq=32, Hkv=8, D=128, DV=128, seqlens_q=[4] * 3,
+                                       seqlens_k=[700, 64, 1000], kv_layout="paged", page_size=64,
+                                       table_width=512, causal=True, descale_mode="per_bkv_uniform",
+                                       seed=309)),
 ]
 
 

@@ -278,3 +278,36 @@ def test_graph_capture_replay_matches_direct(make, splits):
     assert fa8.check() == fa8.FA8_SUCCESS
     assert torch.equal(out.view(torch.int16), out_d.view(torch.int16))
     assert torch.equal(lse, lse_d)
+
+
+# ------------------------------------------------------------------ per-tile split counts
+def test_split_counts_per_tile_varlen_window():
+    """More launched splits than most tiles can use: every tile runs min(n, ceil(t/2))
+    splits of its own key range, and the combine reads exactly those (varlen q: it finds
+    each row's request by binary search)."""
+    case = inputs.make_case(name="spv", B=4, Hq=8, Hkv=2, D=128, DV=128,
+                            seqlens_q=[5, 300, 64, 1], seqlens_k=[900, 300, 2000, 40],
+                            q_layout="varlen", kv_layout="varlen", causal=True, window_left=600,
+                            sink=True, descale_mode="one", seed=151)
+    assert_parity(case, num_splits=16)
+
+
+def test_split_counts_decode_wide_block_table():
+    """Block tables sized for 32k keys, contexts of a few hundred to a few thousand keys: the
+    default heuristic launches many splits, the short requests run few of them."""
+    case = inputs.make_case(name="spw", B=3, Hq=32, Hkv=8, D=128, DV=128, seqlens_q=[1] * 3,
+                            seqlens_k=[300, 4000, 17], kv_layout="paged", page_size=16,
+                            table_width=2048, causal=True, descale_mode="per_bkv_uniform", seed=152)
+    assert_parity(case, num_splits=0)
+
+
+def test_split_path_bit_exact_when_tiles_use_one_split():
+    """Key ranges of at most two 128-key tiles run one split whatever the launch: the 128-row
+    kernel's split path then matches its direct path bit for bit."""
+    case = inputs.make_case(name="sp1", B=2, Hq=8, Hkv=2, D=128, DV=128, seqlens_q=[200] * 2,
+                            seqlens_k=[256] * 2, causal=True, sink=True, seed=153)
+    c = case.to("cuda")
+    o1, l1 = run_gpu(c, num_splits=1)
+    o8, l8 = run_gpu(c, num_splits=8)
+    assert torch.equal(o1.view(torch.int16), o8.view(torch.int16))
+    assert torch.equal(l1, l8)
