@@ -26,6 +26,13 @@ static __device__ __align__(256) unsigned char g_fa8_static_scratch[FA8_STATIC_S
 
 namespace fa8 {
 
+__global__ void split_plan_kernel(const __grid_constant__ FwdParams p) {
+    ptx::griddep_launch_dependents();  // the forward kernel's CTAs may launch meanwhile
+    const int cap = split_tile_cap(p.B, p.Hkv, p.kv_mode, p.Sk, p.cu_k, p.q_varlen, p.Sq, p.cu_q, p.pos_per_tile,
+                                   p.num_splits, p.slots);
+    if (threadIdx.x == 0) *p.split_cap = cap;
+}
+
 __global__ void wait_probe_kernel(unsigned long long timeout_ns, unsigned int *status) {
     __shared__ __align__(8) uint64_t bar;
     __shared__ int abort_flag;
@@ -193,6 +200,7 @@ struct Plan {
     long long max_lk = 0;
     size_t ws_bytes = 0;
     int decode = 0;  // launch decode_kernel (at most 16 rows per kv-head, dv % 128 == 0)
+    long long base_units = 0;  // (tile of query rows, kv-head) pairs, before splitting
 };
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -254,11 +262,11 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
     p.P = 128 / p.G;
     p.rows_per_tile = p.P * p.G;
     // Decode shapes: batched q whose rows per kv-head (Sq x G) fit one 16-row tile.
-    // (Its launch puts the kv-heads and splits on grid x and the requests on grid y, so
-    // that the CTAs of one request, which read neighbouring bytes of the same pages, run
-    // together; grid y is limited to 65535 requests.)
+    // (Its launch puts the kv-heads and then the requests on grid x and the splits on grid
+    // y, so that the CTAs of one request, which read neighbouring bytes of the same pages,
+    // run together.)
     if (g_decode_kernel && q->ndim == 4 && p.DV % 128 == 0 && 16 % p.G == 0 && q->shape[1] * p.G <= 16 &&
-        q->shape[1] > 0 && q->shape[0] <= 65535) {
+        q->shape[1] > 0 && (long long)q->shape[0] * p.Hkv <= 0x7fffffffLL) {
         p.decode = 1;
         p.P = 16 / p.G;
         p.rows_per_tile = 16;
@@ -325,6 +333,7 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
     const long long real_mblocks =
         p.q_varlen ? ((long long)p.total_q + pos_per_slot - 1) / pos_per_slot : p.num_slots;
     const long long base_ctas = std::max(1LL, real_mblocks * p.Hkv);
+    p.base_units = base_ctas;
     const int max_tiles = (int)std::max(1LL, (p.max_lk + 127) / 128);
     int splits;
     if (num_splits == 0) {
@@ -346,9 +355,11 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
     if ((long long)splits * p.Hkv > 65535) return fail(FA8_ERR_UNSUPPORTED, "kv_heads x splits exceeds the grid limit");
     p.splits = splits;
     if (splits > 1 && p.total_q > 0) {
+        // fp32 O and LSE partials, then 256 bytes where the forward kernel records the split
+        // cap it chose for the combine kernel
         const size_t rows = (size_t)p.total_q * p.Hq * splits;
         const size_t o_bytes = (rows * p.DV * sizeof(float) + 255) & ~(size_t)255;
-        p.ws_bytes = o_bytes + ((rows * sizeof(float) + 255) & ~(size_t)255);
+        p.ws_bytes = o_bytes + ((rows * sizeof(float) + 255) & ~(size_t)255) + 256;
     }
     *pl = p;
     return FA8_SUCCESS;
@@ -667,6 +678,13 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
         p.o_part = static_cast<float *>(workspace);
         p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                                ((rows * pl.DV * sizeof(float) + 255) & ~(size_t)255));
+        p.split_cap = reinterpret_cast<int *>(static_cast<char *>(workspace) + pl.ws_bytes - 256);
+        // CTAs that run at once: two decode CTAs per SM for (128, 128), one otherwise
+        const int per_sm = pl.decode ? fa8::decode_ctas_per_sm(pl.D, pl.DV) : 1;
+        p.slots = per_sm * ds->sm_count;
+        // when every launched split fits in one wave the finest cap is always the model's
+        // choice (split_tile_cap): pass it and skip the plan kernel
+        if (pl.base_units * pl.splits <= (long long)p.slots) p.cap_const = 2;
     }
     p.timeout_ns = g_timeout_ns;
     p.status = ds->status;
@@ -675,8 +693,15 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
     const dim3 grid((unsigned)pl.num_slots, (unsigned)(pl.Hkv * pl.splits), 1);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    if (p.split_mode && p.cap_const <= 0) {  // the split cap, chosen on the device from the key counts
+        fa8::split_plan_kernel<<<1, 32, 0, s>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "split plan kernel launch");
+    }
     if (pl.decode) {
-        const dim3 dgrid((unsigned)(pl.Hkv * pl.splits), (unsigned)pl.num_slots, 1);  // see make_plan
+        // kv-heads fastest, then request slots, splits slowest: the CTAs of one request run
+        // side by side, and splits that a request does not use come last and exit at once
+        const dim3 dgrid((unsigned)((long long)pl.Hkv * pl.num_slots), (unsigned)pl.splits, 1);
         switch (pl.D * 1000 + pl.DV) {
             case 128128: e = fa8::launch_decode<128, 128>(p, tq, tk, tv, dgrid, s); break;
             case 192128: e = fa8::launch_decode<192, 128>(p, tq, tk, tv, dgrid, s); break;
@@ -710,6 +735,8 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
         cp.window_left = p.window_left;
         cp.cu_q = p.cu_q;
         cp.cu_k = p.cu_k;
+        cp.split_cap = p.split_cap;
+        cp.cap_const = p.cap_const;
         cp.o_part = p.o_part;
         cp.lse_part = p.lse_part;
         cp.o = p.o;

@@ -146,13 +146,20 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
     const int lane = tid & 31;
 
     // ------------------------------------------------------------ tile schedule (batched q)
-    // grid x = kv-head + Hkv * split (fastest), grid y = request: the CTAs of one request
-    // run side by side and share the L2 lines of its pages
-    const int b = blockIdx.y % p.B;
-    const int mb = blockIdx.y / p.B;
+    // grid x = kv-head + Hkv * slot (kv-heads fastest), grid y = split: the CTAs of one
+    // request run side by side and share the L2 lines of its pages, and the splits a
+    // request does not use (split >= its split count) come last and exit at once
     const int kvh = blockIdx.x % p.Hkv;
-    const int split = blockIdx.x / p.Hkv;
+    const int slot = blockIdx.x / p.Hkv;
+    const int b = slot % p.B;
+    const int mb = slot / p.B;
+    const int split = blockIdx.y;
     const int P = p.pos_per_tile;  // 16 / G positions
+    int cap = p.cap_const > 0 ? p.cap_const : (1 << 20);
+    if (p.num_splits > 1 && p.cap_const <= 0) {  // chosen by split_plan_kernel, which may still be running
+        ptx::griddep_wait();
+        cap = *p.split_cap;
+    }
     const int q_start = b * p.Sq;
     const int Lq = p.Sq;
     int Lk, k_start = 0;
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
     if (pos0 >= Lq) return;
     const int pos_last = min(pos0 + P, Lq) - 1;
     const int delta = Lk - Lq;
-    const SplitRange sr = split_range(Lq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits, split);
+    const SplitRange sr = split_range(Lq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits, cap, split);
     if (split >= sr.eff) return;  // this tile runs fewer splits; the combine skips this one
     const int t_beg = sr.t_beg, n_tiles = sr.n_tiles;
     const bool has_sink = p.sink != nullptr && (!p.split_mode || split == 0);

@@ -103,13 +103,22 @@ struct FwdParams {
     unsigned long long timeout_ns;
     unsigned int *status;
     unsigned long long *trace;  // event timestamps (builds with FA8_TRACE only), may be null
+    // split mode: CTAs that run at once (for split_tile_cap) and the split cap that
+    // split_plan_kernel writes before the forward kernel runs, or, when cap_const > 0, the
+    // cap itself (no plan kernel)
+    int slots;
+    int *split_cap;
+    int cap_const;
 };
 
 struct CombineParams {
     int total_q, Hq, num_splits, q_varlen, Sq;
-    // what the forward kernels derive each row's split count from (see split_range)
+    // what the forward kernels derive each row's split count from (see split_range), and
+    // the split cap split_plan_kernel wrote (cap_const > 0: that cap instead)
     int B, pos_per_tile, kv_mode, Sk, causal, window_left;
     const int *cu_q, *cu_k;
+    const int *split_cap;
+    int cap_const;
     int wpr;  // warps per output row (1, 2, 4 or 8): warp w % wpr takes splits s = w % wpr (mod wpr)
     const float *o_part, *lse_part;
     void *o;
@@ -256,20 +265,18 @@ __device__ __forceinline__ bool tile_needs_mask(int k0, int Lk, int causal, int 
            (window_left >= 0 && k0 < pos_last + delta - window_left);
 }
 
-// Splits of a tile's key range (graph-safe: the launch fixes an upper bound, the device
-// picks the count per tile).  The visible keys of query positions [pos0, pos_last] span KV
-// tiles [tb, te); the tile uses eff = clamp(ceil((te - tb) / kMinTilesPerSplit), 1,
-// num_splits) splits of ceil((te - tb) / eff) tiles each, so a request whose keys are much
-// fewer than the launch was sized for (a block table as wide as the longest request) runs
-// few splits of a useful length instead of many empty or one-tile ones.  Splits >= eff do
-// nothing and the combine kernel, which evaluates the same function per row, never reads
-// them; split 0 always runs (it also writes the result of a tile without visible keys).
-constexpr int kMinTilesPerSplit = 2;
+// Splits of a tile's key range (graph-safe: the launch fixes an upper bound n from shapes
+// only, the device picks what runs).  The visible keys of query positions [pos0, pos_last]
+// span KV tiles [tb, te); the tile runs eff = clamp(ceil((te - tb) / cap), 1, n) splits of
+// ceil((te - tb) / eff) tiles each, where cap (split_tile_cap) is one per launch.  Splits
+// >= eff do nothing and the combine kernel, which evaluates the same function per row with
+// the same cap, never reads them; split 0 always runs (it also writes the result of a tile
+// without visible keys).
 struct SplitRange {
     int t_beg, n_tiles, eff;
 };
 __device__ __forceinline__ SplitRange split_range(int Lq, int Lk, int pos0, int pos_last, int causal,
-                                                  int window_left, int num_splits, int split) {
+                                                  int window_left, int num_splits, int cap, int split) {
     const int delta = Lk - Lq;
     const int kv_end = causal ? min(Lk, pos_last + delta + 1) : Lk;
     const int kv_beg = window_left >= 0 ? max(0, pos0 + delta - window_left) : 0;
@@ -278,13 +285,101 @@ __device__ __forceinline__ SplitRange split_range(int Lq, int Lk, int pos0, int 
         const int tb = kv_beg / kTileN;
         const int te = (kv_end + kTileN - 1) / kTileN;
         const int nt = te - tb;
-        r.eff = max(1, min(num_splits, (nt + kMinTilesPerSplit - 1) / kMinTilesPerSplit));
+        r.eff = max(1, min(num_splits, (nt + cap - 1) / cap));
         const int per = (nt + r.eff - 1) / r.eff;
         r.t_beg = tb + split * per;
         r.n_tiles = max(0, min(te, r.t_beg + per) - r.t_beg);
     }
     return r;
 }
+
+// The largest number of KV tiles a split may take (the cap above), chosen per launch on the
+// device from the requests' key counts, so that it follows the data while the grid stays
+// fixed.  For each candidate cap T (2, 4, ..., 512, and ceil(t_max / n), the finest the
+// launch allows) it counts the work units (tile of query rows, kv-head, split) N(T) and
+// models the run time, in tile times, as
+//   single wave (N <= slots):  F + min(T, t_max)
+//   otherwise:                  (F N + tiles) / slots + beta (F + min(T, t_max))
+// with F the fixed cost of a unit (prologue, pipeline fill and drain, finalize), `tiles` the
+// total KV tile count, t_max the longest request and `slots` the CTAs that run at once: the
+// first term keeps the machine busy, the second is the last units' tail.  F = 3 and
+// beta = 0.4 reproduce the decode kernel's measured times over split counts 1-32 on the
+// mixed-length paged workload and pick the measured best split count of every
+// served-model decode step shape.  Caps that would need more than the launched n splits are
+// skipped.  Each request's tile count is taken from its key count (ceil(Lk / 128)), for
+// every tile of its query rows.  The whole warp calls it and gets the same value in every
+// lane.
+constexpr float kFixedTiles = 3.f, kTailWeight = 0.4f;
+__device__ __forceinline__ int split_tile_cap(int B, int Hkv, int kv_mode, int Sk, const int *cu_k, int q_varlen,
+                                              int Sq, const int *cu_q, int pos_per_tile, int num_splits,
+                                              int slots) {
+    constexpr int NC = 10;  // candidates 2^1 .. 2^9 tiles, then ceil(t_max / n)
+    const int lane = threadIdx.x & 31;
+    // 32-bit counts and fp32 arithmetic only: it runs on the critical path of every split
+    // launch, and the part's FP64 rate is far too low for it
+    unsigned int units[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) units[c] = 0u;
+    unsigned int tiles = 0u;
+    int t_max = 0;
+    // every lane loads its requests' lengths at once (up to kPer per lane in registers, the
+    // rest re-read), the longest request first: it fixes the last candidate
+    constexpr int kPer = 8;
+    int lks[kPer], lqs[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int b = lane + 32 * i;
+        lks[i] = b < B ? (kv_mode == 0 ? Sk : cu_k[b + 1] - cu_k[b]) : 0;
+        lqs[i] = b < B ? (q_varlen ? cu_q[b + 1] - cu_q[b] : Sq) : 0;
+    }
+    auto add_t = [&](int lk) { t_max = max(t_max, lk > 0 ? (lk + kTileN - 1) / kTileN : 0); };
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) add_t(lks[i]);
+    for (int b = lane + 32 * kPer; b < B; b += 32) add_t(kv_mode == 0 ? Sk : cu_k[b + 1] - cu_k[b]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t_max = max(t_max, __shfl_xor_sync(0xffffffffu, t_max, o));
+    const int t_fine = max(2, (t_max + num_splits - 1) / num_splits);
+    auto cand = [&](int c) { return c < NC - 1 ? (2 << c) : t_fine; };
+    auto add_units = [&](int lk, int lq) {
+        const unsigned int t = lk > 0 ? (unsigned int)(lk + kTileN - 1) / kTileN : 0u;
+        const unsigned int mb = lq > 0 ? (unsigned int)(lq + pos_per_tile - 1) / pos_per_tile : 0u;
+        tiles += t * mb;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) units[c] += mb * ((t + (unsigned int)cand(c) - 1u) / (unsigned int)cand(c));
+    };
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) add_units(lks[i], lqs[i]);
+    for (int b = lane + 32 * kPer; b < B; b += 32)
+        add_units(kv_mode == 0 ? Sk : cu_k[b + 1] - cu_k[b], q_varlen ? cu_q[b + 1] - cu_q[b] : Sq);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) units[c] += __shfl_xor_sync(0xffffffffu, units[c], o);
+    }
+    int best_cap = t_fine;  // if no power of two fits n
+    float best = 3.0e38f;
+    const float inv_slots = 1.f / (float)slots;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const int T = cand(c);
+        if (T < t_fine) continue;  // would need more than the launched splits
+        const float n_units = (float)units[c] * (float)Hkv;
+        const float tail = kFixedTiles + (float)min(T, t_max);
+        const float m = n_units <= (float)slots
+                            ? tail
+                            : (kFixedTiles * n_units + (float)tiles * (float)Hkv) * inv_slots + kTailWeight * tail;
+        if (m < best) {
+            best = m;
+            best_cap = T;
+        }
+    }
+    return best_cap;
+}
+
+// One warp: chooses the launch's split cap (split_tile_cap) before the forward kernel runs
+// and leaves it in the workspace for the forward and combine kernels.
+__global__ void split_plan_kernel(const __grid_constant__ FwdParams p);
 
 // Maps a varlen grid slot to (request, slot within the request): the slots enumerate each
 // request's groups of `per_slot` consecutive m-blocks in order; within a request the order
@@ -357,6 +452,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int lane = tid & 31;
 
     // ------------------------------------------------------------ tile schedule
+    int cap = p.cap_const > 0 ? p.cap_const : (1 << 20);
+    if (p.num_splits > 1 && p.cap_const <= 0) {  // chosen by split_plan_kernel, which may still be running
+        ptx::griddep_wait();
+        cap = *p.split_cap;
+    }
     int b, mb;
     if (!p.q_varlen) {
         const int x = blockIdx.x;
@@ -389,7 +489,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (pos0 >= Lq) return;
     const int pos_last = min(pos0 + P, Lq) - 1;
     const int delta = Lk - Lq;
-    const SplitRange sr = split_range(Lq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits, split);
+    const SplitRange sr = split_range(Lq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits, cap, split);
     if (split >= sr.eff) return;  // this tile runs fewer splits; the combine skips this one
     const int t_beg = sr.t_beg, n_tiles = sr.n_tiles;
 
@@ -992,7 +1092,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
         const int Lk = p.kv_mode == 0 ? p.Sk : p.cu_k[b + 1] - p.cu_k[b];
         const int pos0 = pos / p.pos_per_tile * p.pos_per_tile;
         const int pos_last = min(pos0 + p.pos_per_tile, Lq) - 1;
-        ns = split_range(Lq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits, 0).eff;
+        ns = split_range(Lq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits,
+                         p.cap_const > 0 ? p.cap_const : *p.split_cap, 0).eff;
     }
     // every warp reads all the row's split LSEs (a few floats) for the max and the sum
     float m = -INFINITY;

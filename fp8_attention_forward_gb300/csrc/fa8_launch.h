@@ -17,6 +17,16 @@ cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tq, const CUtensor
 template <int DV>
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 
+// CTAs of decode_kernel<D, DV> resident per SM (shared memory decides).
+inline int decode_ctas_per_sm(int D, int DV) {
+    switch (D * 1000 + DV) {
+        case 128128: return DecCfg<128, 128>::CTAS;
+        case 192128: return DecCfg<192, 128>::CTAS;
+        case 256256: return DecCfg<256, 256>::CTAS;
+        default: return 1;
+    }
+}
+
 template <int D, int DV>
 cudaError_t launch_decode(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                           const CUtensorMap &tv, dim3 grid, cudaStream_t stream);
@@ -37,6 +47,26 @@ inline cudaError_t check_launch_regs(K *kernel, int expected, int *cached) {
     return *cached == expected ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
+// Launches a forward kernel.  In split mode split_plan_kernel runs just before it on the
+// same stream, and the forward grid is launched with programmatic stream serialization so
+// that its CTAs start while the plan kernel still runs; they wait for it (griddep_wait)
+// only before reading the split cap it writes.
+template <typename K>
+inline cudaError_t launch_after_plan(K *kernel, const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                                     const CUtensorMap &tv, dim3 grid, int threads, int smem, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (p.split_mode && p.cap_const <= 0) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, p, tq, tk, tv);
+}
+
 // Defines launch_fwd<D, DV>.  Dynamic shared memory above 48 KB needs an opt-in per
 // function and device; it is set on every launch (a cheap host call) so that a first
 // launch on a new device needs no extra bookkeeping.
@@ -49,12 +79,10 @@ inline cudaError_t check_launch_regs(K *kernel, int expected, int *cached) {
         static int regs = -1;                                                                \
         cudaError_t e = check_launch_regs(fwd_kernel<D_, DV_>, kLaunchRegs, &regs);          \
         if (e != cudaSuccess) return e;                                                      \
-        e = cudaFuncSetAttribute(fwd_kernel<D_, DV_>,                                        \
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,    \
-                                             smem);                                          \
+        e = cudaFuncSetAttribute(fwd_kernel<D_, DV_>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 smem);                                                      \
         if (e != cudaSuccess) return e;                                                      \
-        fwd_kernel<D_, DV_><<<grid, kNumThreads, smem, stream>>>(p, tq, tk, tv);             \
-        return cudaGetLastError();                                                           \
+        return launch_after_plan(fwd_kernel<D_, DV_>, p, tq, tk, tv, grid, kNumThreads, smem, stream); \
     }
 
 // Defines launch_decode<D, DV> (the few-rows kernel, dv a multiple of 128).
@@ -68,8 +96,7 @@ inline cudaError_t check_launch_regs(K *kernel, int expected, int *cached) {
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,    \
                                              smem);                                          \
         if (e != cudaSuccess) return e;                                                      \
-        decode_kernel<D_, DV_><<<grid, kDecThreads, smem, stream>>>(p, tq, tk, tv);          \
-        return cudaGetLastError();                                                           \
+        return launch_after_plan(decode_kernel<D_, DV_>, p, tq, tk, tv, grid, kDecThreads, smem, stream); \
     }
 
 }  // namespace fa8

@@ -106,10 +106,14 @@ typedef struct {
  *   range and merge them with a second kernel.  The launch depends only on shapes and the
  *   device's SM count, never on device values, so a call can be graph-captured.  On the
  *   device, a tile whose visible keys span t KV tiles of 128 keys runs
- *   min(n, max(1, ceil(t / 2))) of the launched splits (at least two KV tiles per split);
- *   the other splits exit at once and the merge does not read them.
- * workspace / workspace_bytes: device scratch for the split partials, at least
- *   fa8_fwd_workspace_size() bytes (may be NULL/0 when that size is 0).
+ *   min(n, max(1, ceil(t / cap))) of the launched splits; the other splits exit at once and
+ *   the merge does not read them.  cap (2 to 512 KV tiles per split) is chosen once per
+ *   call from the requests' key counts: the choice that minimises a model of the run time
+ *   (a fixed cost per work unit, the units spread over the CTAs that run at once, and the
+ *   longest unit's tail).
+ * workspace / workspace_bytes: device scratch for the split partials and the split cap the
+ *   forward kernel passes to the merge kernel, at least fa8_fwd_workspace_size() bytes
+ *   (may be NULL/0 when that size is 0).
  */
 FA8_API fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v,
                    const fa8_tensor *descale_q, const fa8_tensor *descale_k,

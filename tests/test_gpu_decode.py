@@ -101,3 +101,47 @@ def test_decode_split_bit_exact_when_one_split_has_keys():
     o4, l4 = run_gpu(c, num_splits=4)
     assert torch.equal(o1.view(torch.int16), o4.view(torch.int16))
     assert torch.equal(l1, l4)
+
+
+def _model_cap(lens, Hkv, n, slots, lens_q=None, P=1):
+    """The split cap the plan kernel should choose (the model restated on the host)."""
+    import math
+    F, BETA = 3.0, 0.4
+    t = [math.ceil(x / 128) if x > 0 else 0 for x in lens]
+    mb = [math.ceil(x / P) if x > 0 else 0 for x in (lens_q or [1] * len(lens))]
+    t_max = max(t)
+    fine = max(2, math.ceil(t_max / n))
+    tiles = sum(a * b for a, b in zip(t, mb))
+    best = None
+    for T in [2 << c for c in range(9)] + [fine]:
+        if T < fine:
+            continue
+        units = Hkv * sum(b * math.ceil(a / T) for a, b in zip(t, mb))
+        tail = F + min(T, t_max)
+        m = tail if units <= slots else (F * units + tiles * Hkv) / slots + BETA * tail
+        if best is None or m < best[0]:
+            best = (m, T)
+    return best[1]
+
+
+@pytest.mark.parametrize("B,ctx,hq,hkv", [(32, 2048, 32, 8), (16, 16384, 32, 8), (64, 4096, 16, 2),
+                                           (8, 32768, 16, 2), (24, None, 16, 2)])
+def test_split_cap_follows_the_key_counts(B, ctx, hq, hkv):
+    """The plan kernel's cap (left in the workspace) is the model's choice for these lengths,
+    and the result still matches the oracle."""
+    lens = [ctx] * B if ctx else inputs.uniform_lengths(B, 1024, 32768, seed=314)
+    case = inputs.make_case(name="cap", B=B, Hq=hq, Hkv=hkv, D=128, DV=128, seqlens_q=[1] * B,
+                            seqlens_k=lens, kv_layout="paged", page_size=16, table_width=2048,
+                            causal=True, descale_mode="per_bkv_uniform", seed=314)
+    c = case.to("cuda")
+    splits, ws_bytes, _ = fa8.plan(c.q, c.k, c.v, cu_seqlens_k=c.cu_seqlens_k, block_table=c.block_table,
+                                   page_size=c.page_size)
+    slots = 2 * torch.cuda.get_device_properties(0).multi_processor_count  # two decode CTAs per SM
+    if splits == 1 or B * hkv * splits <= slots:
+        pytest.skip("this launch takes no plan kernel")
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    run_gpu(c, workspace=ws)
+    cap = int(ws[ws_bytes - 256:ws_bytes - 252].view(torch.int32).item())
+    assert cap == _model_cap(lens, hkv, splits, slots)
+    rows = [(i, h) for i in range(B) for h in (0, hq - 1)]
+    assert_parity(case, rows=rows)
