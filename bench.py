@@ -170,7 +170,17 @@ def bench_case(case, steps, warmup, flush, fa8, num_splits=0):
     st = fa8.check()
     if st != fa8.FA8_SUCCESS:
         raise RuntimeError(f"device status {st}")
-    launches = 1 + (1 if splits > 1 else 0)
+    # forward + combine in split mode, + the split plan kernel unless every launched split
+    # fits in one wave of CTAs (then the host passes the cap and no plan kernel runs)
+    launches = 1
+    if splits > 1:
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        per_sm = 2 if _decode_kernel_name(case).startswith("decode_kernel<128,128>") else 1
+        g = case.Hq // case.Hkv
+        pos = (16 if _decode_kernel_name(case).startswith("decode_kernel") else 128) // g  # positions per tile
+        mblocks = sum((lq + pos - 1) // pos for lq in case.seqlens_q)
+        base = mblocks * case.Hkv
+        launches = 2 + (1 if base * splits > per_sm * sms else 0)
     return {"ms": statistics.mean(times), "ms_min": min(times), "splits": splits,
             "launches_per_step": launches, "out": out, "lse": lse, "ws": ws}
 
