@@ -129,6 +129,9 @@ def test_plan_decode_rows_per_tile(lib):
     # G = 3 does not divide 16: the 128-row kernel (42 positions per tile)
     q, k, v = qkv(B=3, Sq=2, Sk=4096, Hq=6, Hkv=2, D=128, DV=128)
     assert plan(q, k, v, num_splits=1)[2] == (3, 2)
+    # 4 tokens x G = 8 = 32 rows: the 128-row kernel (16 positions per tile, one tile)
+    q, k, v = qkv(B=3, Sq=4, Sk=4096, Hq=16, Hkv=2, D=128, DV=128)
+    assert plan(q, k, v, num_splits=1)[2] == (3, 2)
 
 
 def test_plan_varlen_slots(lib):

@@ -22,7 +22,8 @@ def _built():
 
 
 DECODE = [
-    # (name, kwargs): every shape has Sq * (Hq / Hkv) <= 16 with Hq / Hkv dividing 16
+    # (name, kwargs): Hq / Hkv divides 16; shapes with Sq * (Hq / Hkv) <= 16 run the decode
+    # kernel, the others (marked below) the 128-row kernel either way
     ("g8_paged16_causal", dict(B=4, Hq=16, Hkv=2, D=128, DV=128, seqlens_q=[1] * 4,
                                seqlens_k=[1, 129, 700, 2000], kv_layout="paged", page_size=16,
                                causal=True, descale_mode="per_bkv_uniform", seed=301)),
@@ -42,6 +43,16 @@ DECODE = [
                              descale_mode="tensor_amax", seed=307)),
     ("g8_empty_kv", dict(B=3, Hq=8, Hkv=1, D=128, DV=128, seqlens_q=[1] * 3, seqlens_k=[0, 50, 0],
                          kv_layout="varlen", causal=True, sink=True, seed=308)),
+    # more than 16 rows per kv-head (4 tokens x G 8, 8 x 8, 3 x 8): the 128-row kernel in
+    # both runs, with causal masking across the tokens
+    ("g8_sq4_two_slots", dict(B=3, Hq=16, Hkv=2, D=128, DV=128, seqlens_q=[4] * 3,
+                              seqlens_k=[40, 700, 1300], kv_layout="paged", page_size=16,
+                              causal=True, descale_mode="per_bkv_uniform", seed=315)),
+    ("g8_sq8_four_slots_window_sink", dict(B=2, Hq=8, Hkv=1, D=128, DV=128, seqlens_q=[8] * 2,
+                                           seqlens_k=[600, 2000], kv_layout="paged", page_size=16,
+                                           causal=True, window_left=300, sink=True, seed=316)),
+    ("g8_sq3_ragged_slot_d256", dict(B=2, Hq=8, Hkv=1, D=256, DV=256, seqlens_q=[3] * 2,
+                                     seqlens_k=[3, 900], kv_layout="varlen", causal=True, seed=317)),
     # four query tokens per request, GQA 32/8, 64-token pages in a table as wide as 32k keys
     ("g4_sq4_paged64_wide_table", dict(B=3, Hq=32, Hkv=8, D=128, DV=128, seqlens_q=[4] * 3,
                                        seqlens_k=[700, 64, 1000], kv_layout="paged", page_size=64,
