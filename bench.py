@@ -185,12 +185,15 @@ def bench_case(case, steps, warmup, flush, fa8, num_splits=0):
             "launches_per_step": launches, "out": out, "lse": lse, "ws": ws}
 
 
+E2E_SETS = 3  # buffer sets of the end-to-end pipeline
+
+
 def bench_e2e(case, steps, warmup, flush, fa8, num_splits=0):
     """End-to-end through the public call: every step copies its inputs (Q/K/V and the small
     index tensors) from pinned host memory, runs the forward and copies O and LSE back to
-    pinned host memory.  Two buffer sets and three streams let the copies of neighbouring
-    steps overlap the forward of the current one (H2D of step i+1 and D2H of step i-1 run
-    while step i computes), as a serving loop would; every step's copies are inside the
+    pinned host memory.  E2E_SETS buffer sets and three streams let the copies of
+    neighbouring steps overlap the forward of the current one (H2D of the next steps and D2H
+    of the previous ones run while step i computes), as a serving loop would; every step's copies are inside the
     timed region, which runs from the first H2D to the last D2H.  The L2 flush is issued on
     the compute stream before every forward.  Returns the pipelined and the serial time per
     step."""
@@ -204,7 +207,7 @@ def bench_e2e(case, steps, warmup, flush, fa8, num_splits=0):
         if t is not None:
             host[n] = t.cpu().pin_memory()
     sets = []
-    for _ in range(2):
+    for _ in range(E2E_SETS):
         dst = {n: torch.empty_like(getattr(case, n)) for n in host}
         dcase = dataclasses.replace(case, **dst)
         out = torch.empty(tuple(dcase.q.shape[:-1]) + (dcase.DV,), dtype=dcase.out_dtype, device="cuda")
@@ -216,7 +219,7 @@ def bench_e2e(case, steps, warmup, flush, fa8, num_splits=0):
     c0 = sets[0]["case"]
     splits, ws_bytes, _ = fa8.plan(c0.q, c0.k, c0.v, cu_seqlens_q=c0.cu_seqlens_q, cu_seqlens_k=c0.cu_seqlens_k,
                                    block_table=c0.block_table, page_size=c0.page_size, num_splits=num_splits)
-    ws = [torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    ws = [torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") for _ in range(E2E_SETS)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sets[0]["out"].numel() * sets[0]["out"].element_size() + sets[0]["lse"].numel() * sets[0]["lse"].element_size()
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
@@ -229,19 +232,19 @@ def bench_e2e(case, steps, warmup, flush, fa8, num_splits=0):
         torch.cuda.synchronize()
         t0.record(s_in)
         for i in range(n):
-            S = sets[i % 2]
+            S = sets[i % E2E_SETS]
             with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(ev_cmp[i - 2])  # inputs of set i%2 consumed by step i-2
+                if i >= E2E_SETS:
+                    s_in.wait_event(ev_cmp[i - E2E_SETS])  # this set's inputs consumed by its last step
                 for k_, t in host.items():
                     S["dst"][k_].copy_(t, non_blocking=True)
                 ev_in[i].record(s_in)
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(ev_in[i])
-                if i >= 2:
-                    s_cmp.wait_event(ev_out[i - 2])  # outputs of set i%2 read back by step i-2
+                if i >= E2E_SETS:
+                    s_cmp.wait_event(ev_out[i - E2E_SETS])  # this set's outputs read back by its last step
                 flush.fill_(1)
-                fa8.fwd_case(S["case"], out=S["out"], lse=S["lse"], workspace=ws[i % 2], num_splits=num_splits,
+                fa8.fwd_case(S["case"], out=S["out"], lse=S["lse"], workspace=ws[i % E2E_SETS], num_splits=num_splits,
                              stream=s_cmp)
                 ev_cmp[i].record(s_cmp)
             with torch.cuda.stream(s_out):
@@ -449,7 +452,7 @@ def main():
                          "peak_source": f"{peaks['source']} bf16 burst x2 (dense FP8 = 2x bf16)"},
             "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e_ms,
-                    "mode": "pipelined: 2 buffer sets, copy-in / compute / copy-out streams",
+                    "mode": f"pipelined: {E2E_SETS} buffer sets, copy-in / compute / copy-out streams",
                     "ms_per_step_serial": e2e["ms_serial"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
             "clocks": clk, "decode": decode, "cpu_baseline": cpu, "wall_s_timed_region": wall,
