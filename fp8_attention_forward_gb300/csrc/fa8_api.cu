@@ -54,8 +54,18 @@ __global__ void wait_probe_kernel(unsigned long long timeout_ns, unsigned int *s
         const long long rows = (long long)p.total_q * p.Hq;                                 \
         const long long per_cta = 8 / p.wpr;                                                \
         const unsigned blocks = (unsigned)((rows + per_cta - 1) / per_cta);                 \
-        combine_kernel<DV_><<<blocks, 256, 0, s>>>(p);                                      \
-        return cudaGetLastError();                                                          \
+        /* programmatic dependent launch: the merge's CTAs start while the forward        \
+           kernel drains and wait for it (griddep_wait) before reading anything */        \
+        cudaLaunchConfig_t cfg = {};                                                        \
+        cfg.gridDim = dim3(blocks, 1, 1);                                                   \
+        cfg.blockDim = dim3(256, 1, 1);                                                     \
+        cfg.stream = s;                                                                     \
+        cudaLaunchAttribute attr[1];                                                        \
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;                    \
+        attr[0].val.programmaticStreamSerializationAllowed = 1;                             \
+        cfg.attrs = attr;                                                                   \
+        cfg.numAttrs = 1;                                                                   \
+        return cudaLaunchKernelEx(&cfg, combine_kernel<DV_>, p);                            \
     }
 FA8_DEFINE_COMBINE(64)
 FA8_DEFINE_COMBINE(96)

@@ -1071,6 +1071,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
     const long long stride_s = rows;
     const int tok = (int)(row / p.Hq);
     const int hq = (int)(row % p.Hq);
+    // this grid may start while the forward kernel ahead of it drains (programmatic
+    // dependent launch): its partials are complete and visible past this point
+    ptx::griddep_wait();
     // the splits the forward ran for this row's tile (split_range on the same inputs)
     int ns = 1;
     if (active) {
