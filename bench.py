@@ -40,10 +40,10 @@ METRIC = "FP8 attn fwd TFLOP/s (prefill) & decode HBM GB/s; % of GB300 roofline"
 # DRAM bytes (read + write) per launch from one ncu capture of each timed kernel (summaries
 # under profiles/), valid only while the kernel sources hash to the value recorded with it.
 PROFILED_TRAFFIC = {
-    "prefill": {"kernel": "fwd_kernel<128,128>", "bytes": 68.77e6,
-                "sources": ["fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "05d0576c14ef8a51"},
-    "decode": {"kernel": "decode_kernel<128,128>", "bytes": 2074.2e6,
-               "sources": ["fa8_decode.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "8c9e4122f8e22230"},
+    "prefill": {"kernel": "fwd_kernel<128,128>", "bytes": 68.83e6,
+                "sources": ["fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "480053e2631e1a2c"},
+    "decode": {"kernel": "decode_kernel<128,128>", "bytes": 2073.9e6,
+               "sources": ["fa8_decode.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "b0d0974e69d9882e"},
 }
 
 

@@ -174,10 +174,14 @@ struct Cfg {
     static constexpr int B_PF = B_SF + NS;
     static constexpr int B_OF = B_PF + NS;   // NOT slots
     static constexpr int B_OE = B_OF + NOT;  // NOT slots
-    static constexpr int NA = 4;             // alpha ring depth (softmax -> correction)
+    // Alpha ring depth (softmax -> correction).  The ring needs no "slot empty" barrier: the
+    // softmax writes the slot of tile t only after S(t) is ready, which follows the issue of
+    // QK(t), which follows the issue of PV(t - 1) or PV(t - 2), which waits for the fold of
+    // an O_tile from tile t - 2 or earlier; the correction reads a tile's alpha before it
+    // folds that tile, so the slot's previous tile (t - 4) has been read.
+    static constexpr int NA = 4;
     static constexpr int B_AF = B_OE + NOT;  // NA slots
-    static constexpr int B_AE = B_AF + NA;   // NA slots
-    static constexpr int B_XCH = B_AE + NA;  // 2 slots: row-max exchange between the halves
+    static constexpr int B_XCH = B_AF + NA;  // 2 slots: row-max exchange between the halves
     static constexpr int B_SUM = B_XCH + 2;  // half 1 -> half 0: final partial row sums
     static constexpr int B_FIN = B_SUM + 1;  // half 0 -> correction: final O scale
     static constexpr int B_DONE = B_FIN + 1;
@@ -555,7 +559,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         for (int i = 0; i < C::NA; ++i) {
             ptx::mbar_init(BAR(C::B_AF + i), 128);
-            ptx::mbar_init(BAR(C::B_AE + i), 128);
         }
         for (int i = 0; i < 2; ++i) ptx::mbar_init(BAR(C::B_XCH + i), 256);
         ptx::mbar_init(BAR(C::B_SUM), 128);
@@ -871,7 +874,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (tid == 0) FA8_EV(5, it);
             if (h == 0) {
                 const int as = it % C::NA;
-                if (!W.wait_warp(BAR(C::B_AE + as), ((uint32_t)(it / C::NA) & 1u) ^ 1u)) break;
                 alpha_ring[as * 128 + r] = alpha;
                 ptx::mbar_arrive(BAR(C::B_AF + as));
                 if (tid == 0) FA8_EV(6, it);
@@ -923,7 +925,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const int as = it % C::NA;
             if (!W.wait_warp(BAR(C::B_AF + as), (uint32_t)(it / C::NA) & 1u)) break;
             const float alpha = alpha_ring[as * 128 + r];
-            ptx::mbar_arrive(BAR(C::B_AE + as));
 #pragma unroll
             for (int c = 0; c < C::NPV; ++c) {
                 const int ob = pv_uses % C::NOT;
