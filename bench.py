@@ -40,10 +40,10 @@ METRIC = "FP8 attn fwd TFLOP/s (prefill) & decode HBM GB/s; % of GB300 roofline"
 # DRAM bytes (read + write) per launch from one ncu capture of each timed kernel (summaries
 # under profiles/), valid only while the kernel sources hash to the value recorded with it.
 PROFILED_TRAFFIC = {
-    "prefill": {"kernel": "fwd_kernel<128,128>", "bytes": 68.83e6,
-                "sources": ["fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "480053e2631e1a2c"},
-    "decode": {"kernel": "decode_kernel<128,128>", "bytes": 2073.9e6,
-               "sources": ["fa8_decode.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "b0d0974e69d9882e"},
+    "prefill": {"kernel": "fwd_kernel<128,128>", "bytes": 68.41e6,
+                "sources": ["fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "92e86360ee36f6f1"},
+    "decode": {"kernel": "decode_kernel<128,128>", "bytes": 2073.6e6,
+               "sources": ["fa8_decode.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "a855ada72c561ba6"},
 }
 
 

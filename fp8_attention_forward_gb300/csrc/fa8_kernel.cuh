@@ -49,7 +49,14 @@ constexpr int kRegsSoft = 112;
 constexpr int kRegsCorr = 240;
 constexpr int kRegsCtl = 48;
 static_assert(2 * kRegsSoft + kRegsCorr + kRegsCtl == 4 * kLaunchRegs, "register split");
-constexpr float kTau = 0.75f;   // lazy-rescale threshold, log2 units
+// Lazy-rescale threshold, log2 units: the running max moves only when a tile's max passes it
+// by more than this, so it must stay below log2(448) - 8 for P = 2^(s c - m + 8) to fit
+// E4M3.  FA8_TAU overrides it only for the negative-control build of the threshold test.
+#ifdef FA8_TAU
+constexpr float kTau = FA8_TAU;
+#else
+constexpr float kTau = 0.75f;
+#endif
 constexpr float kPBias = 8.0f;  // P carries a factor 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

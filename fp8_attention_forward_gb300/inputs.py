@@ -388,6 +388,45 @@ def decode_step(shape, device="cpu", max_seqlen_k=32768) -> Case:
                      out_dtype=torch.bfloat16, seed=5, device=device)
 
 
+STAIRCASE_Q_LEVELS = (1.0, 1.25, 1.5, 1.75)  # exact E4M3 values
+
+
+def lazy_staircase(kind="prefill", device="cpu", tiles=64) -> Case:
+    """Scores that climb steadily along the keys, to exercise the lazy rescale threshold.
+
+    Every row's largest score rises by 0.5 q log2-units per 128 keys for ``tiles`` blocks of
+    128 keys, so an online softmax that moves its running max only after the block max has
+    passed it by more than a threshold writes unnormalised weights up to 2^threshold: above
+    the E4M3 range once the threshold exceeds log2(448) - 8.  Built from exact E4M3 values:
+    Q rows are constant vectors of one of STAIRCASE_Q_LEVELS (cycling over rows and heads);
+    key j of block t has n = max(0, 2 t - 3 (j mod 8)) leading components equal to 2 and
+    the rest 0; with softmax_scale = ln 2 / 8 its log2-unit score is q n / 4.  V is
+    e4m3(N(0,1)), seed 6.  ``kind`` "prefill": 64 query rows, 2 q-heads on one kv-head
+    (the 128-row kernel); "decode": two one-token requests with 8 q-heads on one kv-head
+    (the decode kernel).
+    """
+    if kind == "prefill":
+        B, Sq, Hq = 1, 64, 2
+    else:
+        B, Sq, Hq = 2, 1, 8
+    D = DV = 128
+    sk = tiles * 128
+    lev = torch.tensor(STAIRCASE_Q_LEVELS, dtype=torch.float32)
+    idx = (torch.arange(Sq)[:, None] * Hq + torch.arange(Hq)[None, :]) % len(STAIRCASE_Q_LEVELS)
+    q = lev[idx][None, :, :, None].expand(B, Sq, Hq, D).contiguous()
+    j = torch.arange(sk)
+    n = (2 * (j // 128) - 3 * (j % 8)).clamp_min(0)
+    k = (torch.arange(D)[None, :] < n[:, None]).to(torch.float32) * 2.0
+    k = k[None, :, None, :].expand(B, sk, 1, D).contiguous()
+    gen = torch.Generator().manual_seed(6)
+    v, _ = _quantised_payload((B, sk, 1, DV), gen, "cpu", 6, 3, 0.0, 1.0, "one")
+    case = Case(name=f"lazy_staircase_{kind}", B=B, Hq=Hq, Hkv=1, D=D, DV=DV,
+                seqlens_q=[Sq] * B, seqlens_k=[sk] * B, q_layout="batched", kv_layout="batched",
+                q=quantise_e4m3(q, None), k=quantise_e4m3(k, None), v=v,
+                softmax_scale=math.log(2.0) / 8.0, out_dtype=torch.bfloat16)
+    return case.to(device)
+
+
 def algorithmic_flops(case: Case) -> float:
     """2*(d+dv) flops per unmasked (row, key) pair, summed over heads."""
     return 2.0 * (case.D + case.DV) * case.pairs()

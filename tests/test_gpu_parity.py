@@ -7,6 +7,9 @@ tiling is identical: paged vs contiguous K/V, and the split/combine path vs the 
 path when only the first split has keys.
 """
 import dataclasses
+import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -58,6 +61,41 @@ def test_long_kv_small(sq, splits):
 
 def test_varlen_swa_prefill_small():
     assert_parity(inputs.varlen_swa_prefill("small"))
+
+
+# ------------------------------------------------------------------ lazy rescale threshold
+@pytest.mark.parametrize("kind", ["prefill", "decode"])
+def test_lazy_rescale_staircase(kind):
+    """Scores rising 0.5 q log2-units per 128 keys over 64 tiles, walked by one CTA (one
+    split: the split heuristic would cut the staircase into short pieces): with the
+    threshold 0.75 (below log2(448) - 8) no weight leaves the E4M3 range and the output
+    meets the bar."""
+    assert_parity(inputs.lazy_staircase(kind), num_splits=1)
+
+
+def test_lazy_threshold_negative_control(tmp_path):
+    """The same staircase through a build whose threshold is 4 (above log2(448) - 8): weights
+    up to 2^12 saturate at 448 and the output misses the bar by a wide margin, so the
+    staircase test does depend on the threshold."""
+    lib = build.build(out_dir=str(tmp_path / "tau4"), defines=["FA8_TAU=4.0f"])
+    out_file = tmp_path / "out.pt"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = (
+        "import sys, torch\n"
+        f"sys.path.insert(0, {root!r})\n"
+        "from fp8_attention_forward_gb300 import fa8, inputs\n"
+        "c = inputs.lazy_staircase('prefill', device='cuda')\n"
+        "out, lse = fa8.fwd_case(c, num_splits=1)\n"
+        "assert fa8.check() == fa8.FA8_SUCCESS\n"
+        f"torch.save((out.cpu(), lse.cpu()), {str(out_file)!r})\n")
+    subprocess.run([sys.executable, "-c", script], env=dict(os.environ, FA8_LIBRARY=lib),
+                   check=True, timeout=600)
+    out, lse = torch.load(out_file)
+    case = inputs.lazy_staircase("prefill")
+    o, l = gpu_outputs(case, out, lse)
+    o_ref, l_ref = oracle.attention(case)
+    mx, mean, le = errors(case, o, l, o_ref, l_ref)
+    assert mx > 2 * MAX_ABS and mean > 2 * MEAN_ABS, (mx, mean, le)
 
 
 # ------------------------------------------------------------------ feature matrix
