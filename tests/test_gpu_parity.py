@@ -287,9 +287,14 @@ def test_wait_timeout_is_reported():
 
 
 # ------------------------------------------------------------------ CUDA graph capture
+def _step_128x1_1k():
+    return inputs.decode_step(next(s for s in inputs.DECODE_STEP_SHAPES if s[1] == 128 and s[3] == 1024))
+
+
 @pytest.mark.parametrize("make,splits", [(lambda: inputs.causal_gqa_prefill("small"), 0),
-                                         (lambda: inputs.paged_decode("small"), 3)],
-                         ids=["prefill", "decode_split3"])
+                                         (lambda: inputs.paged_decode("small"), 3),
+                                         (_step_128x1_1k, 0)],
+                         ids=["prefill", "decode_split3", "decode_step_plan_kernel"])
 def test_graph_capture_replay_matches_direct(make, splits):
     """Launch choices depend only on shapes, so a call captured in a CUDA graph replays to
     the same bits as a direct call (workspace, outputs and inputs at fixed addresses)."""
