@@ -355,10 +355,33 @@ def pin_nonzero_mean_v(mutant):
     return abs(float(o.mean()) / dv * dv - 1.0) < 0.02
 
 
+def pin_split_merge(mutant):
+    """Keys split into a prefix and the rest: merging the two partial results by their LSEs
+    (LSE = log(e^LSE_1 + e^LSE_2), O = sum_s e^(LSE_s - LSE) O_s, in fp64) gives the single
+    pass.  The sink goes with one part only."""
+    import dataclasses
+
+    case = _mk(B=1, Hq=2, Hkv=1, seqlens_q=[4], seqlens_k=[11], seed=30, sink=True,
+               descale_mode="per_bkv_uniform")
+    o, l = oracle.attention(case, mutant=mutant)
+    a = 4
+    k8, v8 = case.k.view(torch.uint8), case.v.view(torch.uint8)
+    part = lambda t: t.contiguous().view(torch.float8_e4m3fn)
+    c1 = dataclasses.replace(case, seqlens_k=[a], k=part(k8[:, :a]), v=part(v8[:, :a]))
+    c2 = dataclasses.replace(case, seqlens_k=[11 - a], k=part(k8[:, a:]), v=part(v8[:, a:]),
+                             sink=None)
+    o1, l1 = oracle.attention(c1, mutant=mutant)
+    o2, l2 = oracle.attention(c2, mutant=mutant)
+    lm = np.logaddexp(l1, l2)
+    om = np.exp(l1 - lm)[..., None] * o1 + np.exp(l2 - lm)[..., None] * o2
+    return _close(om, o, 1e-12) and _close(lm, l, 1e-12)
+
+
 PINS = [pin_e4m3_torch, pin_e4m3_golden, pin_brute_force, pin_constant_v,
         pin_rows_sum_to_one, pin_equal_keys, pin_causal_first_row, pin_zero_window,
         pin_permutation, pin_gqa_equals_mha, pin_varlen_equals_dense,
-        pin_paged_equals_contiguous, pin_descale_structure, pin_nonzero_mean_v]
+        pin_paged_equals_contiguous, pin_descale_structure, pin_nonzero_mean_v,
+        pin_split_merge]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
