@@ -358,6 +358,37 @@ def decode_steps_suite(args):
         del case, r, eager
 
 
+def configs_suite(args):
+    """Times the forward on every configured workload (L2 flushed before every step) and
+    prints one JSON line each with its roofline fraction: tensor-bound workloads in TFLOP/s
+    against the dense FP8 peak, HBM-bound ones in GB/s against the copy bandwidth."""
+    import torch
+
+    from fp8_attention_forward_gb300 import fa8
+
+    peaks = _peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    work = [("causal GQA prefill", lambda: inputs.causal_gqa_prefill("full", device="cuda"), "tensor"),
+            ("paged decode", lambda: inputs.paged_decode("full", device="cuda"), "hbm"),
+            ("long-KV, 1 query row", lambda: inputs.long_kv(1, "full", device="cuda"), "hbm"),
+            ("long-KV, 128 query rows", lambda: inputs.long_kv(128, "full", device="cuda"), "tensor"),
+            ("varlen sliding-window prefill", lambda: inputs.varlen_swa_prefill("full", device="cuda"), "tensor")]
+    for name, make, bound in work:
+        case = make()
+        r = bench_case(case, args.steps, args.warmup, flush, fa8)
+        sec = r["ms"] * 1e-3
+        if bound == "tensor":
+            val, unit, peak = inputs.algorithmic_flops(case) / sec / 1e12, "TFLOP/s", fp8_peak
+        else:
+            val, unit, peak = inputs.algorithmic_bytes(case) / sec / 1e9, "GB/s", peaks["hbm_gbs"]
+        print(json.dumps({"suite": "configs", "workload": case.name, "what": name, "us": r["ms"] * 1e3,
+                          "value": val, "unit": unit, "bound": bound, "peak": peak, "frac": val / peak,
+                          "splits": r["splits"], "steps": args.steps, "warmup": args.warmup,
+                          "l2": "256 MB buffer written before every step"}))
+        del case, r
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -366,12 +397,16 @@ def main():
     ap.add_argument("--impl", default="fa8", choices=["fa8", "reference"])
     ap.add_argument("--no-decode", action="store_true", help="skip the paged-decode figure")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--suite", default="", choices=["", "decode-steps"],
+    ap.add_argument("--suite", default="", choices=["", "decode-steps", "configs"],
                     help="decode-steps: one JSON line per served-model decode step shape "
-                         "(kernel time incl. the split combine) instead of the headline line")
+                         "(kernel time incl. the split combine); configs: one line per "
+                         "configured workload with its roofline fraction; both instead of "
+                         "the headline line")
     args = ap.parse_args()
     if args.suite == "decode-steps":
         return decode_steps_suite(args)
+    if args.suite == "configs":
+        return configs_suite(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
