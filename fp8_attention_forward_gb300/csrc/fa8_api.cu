@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -78,9 +79,11 @@ FA8_DEFINE_COMBINE(256)
 namespace {
 
 thread_local std::string g_last_error;
-unsigned long long g_timeout_ns = 2000000000ull;
-unsigned long long *g_trace = nullptr;  // pipeline trace buffer (FA8_TRACE builds)
-bool g_decode_kernel = true;            // few-rows shapes go to decode_kernel
+// Process-wide settings, written by the setters and read once per fa8_fwd call; atomics, so
+// that a setter on one host thread and a forward call on another never race.
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<unsigned long long *> g_trace{nullptr};  // pipeline trace buffer (FA8_TRACE builds)
+std::atomic<bool> g_decode_kernel{true};             // few-rows shapes go to decode_kernel
 
 fa8_status fail(fa8_status s, const char *fmt, ...) {
     char buf[512];
@@ -240,7 +243,7 @@ fa8_status check_payload(const fa8_tensor *t, const char *name) {
 
 fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v, const fa8_tensor *cu_q,
                      const fa8_tensor *cu_k, const fa8_tensor *bt, int page_size, int num_splits, int sm_count,
-                     Plan *pl) {
+                     bool use_decode, Plan *pl) {
     if (!q || !k || !v) return fail(FA8_ERR_INVALID_ARG, "q, k and v are required");
     for (const fa8_tensor *t : {q, k, v}) {
         if (t->dtype == FA8_DTYPE_E5M2) return fail(FA8_ERR_UNSUPPORTED, "E5M2 inputs are not supported (E4M3 only)");
@@ -275,7 +278,7 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
     // (Its launch puts the kv-heads and then the requests on grid x and the splits on grid
     // y, so that the CTAs of one request, which read neighbouring bytes of the same pages,
     // run together.)
-    if (g_decode_kernel && q->ndim == 4 && p.DV % 128 == 0 && 16 % p.G == 0 && q->shape[1] * p.G <= 16 &&
+    if (use_decode && q->ndim == 4 && p.DV % 128 == 0 && 16 % p.G == 0 && q->shape[1] * p.G <= 16 &&
         q->shape[1] > 0 && (long long)q->shape[0] * p.Hkv <= 0x7fffffffLL) {
         p.decode = 1;
         p.P = 16 / p.G;
@@ -417,13 +420,13 @@ const char *fa8_status_string(fa8_status s) {
 fa8_status fa8_set_decode_kernel(int enable) {
     g_last_error.clear();
     if (enable != 0 && enable != 1) return fail(FA8_ERR_INVALID_ARG, "enable must be 0 or 1");
-    g_decode_kernel = enable == 1;
+    g_decode_kernel.store(enable == 1);
     return FA8_SUCCESS;
 }
 
 fa8_status fa8_set_wait_timeout_ns(uint64_t ns) {
     if (ns < 100000ull) return fail(FA8_ERR_INVALID_ARG, "timeout must be >= 1e5 ns");
-    g_timeout_ns = ns;
+    g_timeout_ns.store(ns);
     return FA8_SUCCESS;
 }
 
@@ -434,8 +437,8 @@ fa8_status fa8_fwd_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tens
     g_last_error.clear();
     if (sm_count <= 0) return fail(FA8_ERR_INVALID_ARG, "sm_count must be positive");
     Plan pl;
-    fa8_status st =
-        make_plan(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, sm_count, &pl);
+    fa8_status st = make_plan(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, sm_count,
+                              g_decode_kernel.load(), &pl);
     if (st) return st;
     if (splits_out) *splits_out = pl.splits;
     if (bytes_out) *bytes_out = pl.ws_bytes;
@@ -452,11 +455,14 @@ fa8_status fa8_fwd_workspace_size(const fa8_tensor *q, const fa8_tensor *k, cons
                                   size_t *bytes_out) {
     g_last_error.clear();
     Plan pl;
-    fa8_status st = make_plan(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, 1, &pl);
+    const bool use_decode = g_decode_kernel.load();
+    fa8_status st =
+        make_plan(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, 1, use_decode, &pl);
     if (st) return st;
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds))) return st;
-    st = make_plan(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, ds->sm_count, &pl);
+    st = make_plan(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, ds->sm_count, use_decode,
+                   &pl);
     if (st) return st;
     if (splits_out) *splits_out = pl.splits;
     if (bytes_out) *bytes_out = pl.ws_bytes;
@@ -468,14 +474,17 @@ fa8_status fa8_check(void *stream) {
     DeviceState *ds = nullptr;
     fa8_status st = device_state(&ds);
     if (st) return st;
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    // everything on the caller's stream: the read is ordered after the work enqueued there,
+    // and no other stream is waited for
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned int word = 0;
-    e = cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost);
+    cudaError_t e = cudaMemcpyAsync(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     if (word) {
-        const unsigned int zero = 0;
-        e = cudaMemcpy(ds->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        e = cudaMemsetAsync(ds->status, 0, sizeof(unsigned int), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
     }
     if (word & fa8::kStatusTimeout) return fail(FA8_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
@@ -488,7 +497,7 @@ fa8_status fa8_debug_set_trace_buffer(void *device_buffer, size_t bytes) {
 #ifdef FA8_TRACE
     const size_t need = sizeof(unsigned long long) * fa8::kTraceCtas * fa8::kTraceEvents * fa8::kTraceTiles;
     if (device_buffer && bytes < need) return fail(FA8_ERR_INVALID_ARG, "trace buffer needs %zu bytes", need);
-    g_trace = static_cast<unsigned long long *>(device_buffer);
+    g_trace.store(static_cast<unsigned long long *>(device_buffer));
     return FA8_SUCCESS;
 #else
     (void)device_buffer;
@@ -502,7 +511,7 @@ fa8_status fa8_debug_wait_probe(void *stream) {
     DeviceState *ds = nullptr;
     fa8_status st = device_state(&ds);
     if (st) return st;
-    fa8::wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(g_timeout_ns, ds->status);
+    fa8::wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(g_timeout_ns.load(), ds->status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
     return fa8_check(stream);
@@ -515,8 +524,13 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
                    int num_splits, void *workspace, size_t workspace_bytes, void *stream) {
     g_last_error.clear();
     Plan pl;
+    // the settings are read once, so one call sees one consistent set of them
+    const bool use_decode = g_decode_kernel.load();
+    const unsigned long long timeout_ns = g_timeout_ns.load();
+    unsigned long long *const trace = g_trace.load();
     // shape validation first (host only), then the device-dependent plan
-    fa8_status st = make_plan(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, 1, &pl);
+    fa8_status st =
+        make_plan(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, 1, use_decode, &pl);
     if (st) return st;
 
     // ---- output
@@ -577,7 +591,8 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
     // ---- device-dependent plan (split count from the SM count)
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds))) return st;
-    st = make_plan(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, ds->sm_count, &pl);
+    st = make_plan(q, k, v, cu_seqlens_q, cu_seqlens_k, block_table, page_size, num_splits, ds->sm_count, use_decode,
+                   &pl);
     if (st) return st;
     if (pl.splits > 1) {
         if (!workspace || workspace_bytes < pl.ws_bytes)
@@ -696,9 +711,9 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
         // choice (split_tile_cap): pass it and skip the plan kernel
         if (pl.base_units * pl.splits <= (long long)p.slots) p.cap_const = 2;
     }
-    p.timeout_ns = g_timeout_ns;
+    p.timeout_ns = timeout_ns;
     p.status = ds->status;
-    p.trace = g_trace;
+    p.trace = trace;
 
     const dim3 grid((unsigned)pl.num_slots, (unsigned)(pl.Hkv * pl.splits), 1);
     cudaStream_t s = static_cast<cudaStream_t>(stream);

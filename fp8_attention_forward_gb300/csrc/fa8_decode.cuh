@@ -3,9 +3,13 @@
 //
 // Same arithmetic as fwd_kernel (online exp2 softmax with the descales folded into the
 // scale, P in E4M3 with a 2^8 bias, lazy rescale with tau = 0.75, two-level PV
-// accumulation, two-term P on masked tiles, sink and LSE at finalize), but the tile is
-// transposed so that the 128 keys of a KV tile lie along the MMA's M dimension (TMEM
-// lanes) and the query rows along N = 16:
+// accumulation, sink and LSE at finalize), except that every tile's P goes through the PV
+// MMA as two E4M3 terms, P_hi + P_lo with P_lo = e4m3(p - P_hi): decode rows often hold a
+// few keys that carry most of the softmax mass, where one E4M3 term (up to 2^-4 relative
+// rounding of a dominant weight) can put the output past the stated error bar; the second
+// term costs one more small PV MMA and the P_lo stores, which this HBM-bound kernel hides.
+// The tile is transposed so that the 128 keys of a KV tile lie along the MMA's M dimension
+// (TMEM lanes) and the query rows along N = 16:
 //
 //   S^T (128 keys x 16 rows)  = K (128 x d, K-major smem)  .  Q^T (Q: 16 x d, K-major smem)
 //   O^T (dv x 16 rows)       += V^T (V: 128 x dv smem, MN-major A operand) . P^T (16 x 128)
@@ -372,7 +376,8 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
             if (!W.wait_warp(BAR(C::B_VF + vs), (uint32_t)(j / C::STAGES) & 1u)) return false;
             if (!W.wait_warp(BAR(C::B_OE + pb), ((uint32_t)(j >> 1) & 1u) ^ 1u)) return false;
             ptx::tc_fence_after();
-            const bool two_term = tile_needs_mask((t_beg + j) * kTileN, Lk, p.causal, p.window_left, pos0, pos_last, delta);
+            // every tile takes the second P term (see the softmax)
+            constexpr bool two_term = true;
             const uint64_t dv = dv0 + (uint64_t)((vs * C::V_BYTES) >> 4);
             const uint64_t dp = dp0 + (uint64_t)((pb * 2 * C::P_BYTES) >> 4);
             if (leader) {
@@ -503,7 +508,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
                 const uint32_t h = ptx::cvt_e4m3x2(p1, p0);
                 ptx::st_shared_u8(phi + swz128_offset(q, t), h & 0xFFu);
                 ptx::st_shared_u8(phi + swz128_offset(q + 1, t), h >> 8);
-                if (need_mask) {  // second E4M3 term: P_lo = e4m3(p - P_hi)
+                {  // second E4M3 term on every tile: P_lo = e4m3(p - P_hi)
                     float q0, q1;
                     ptx::e4m3x2_to_f32(h, q0, q1);
                     const uint32_t l = ptx::cvt_e4m3x2(p1 - q1, p0 - q0);

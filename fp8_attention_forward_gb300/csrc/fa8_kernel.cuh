@@ -58,6 +58,12 @@ constexpr float kTau = FA8_TAU;
 constexpr float kTau = 0.75f;
 #endif
 constexpr float kPBias = 8.0f;  // P carries a factor 2^8
+// A tile's P goes through the PV MMA as two E4M3 terms (P_hi + P_lo, P_lo = e4m3(p - P_hi))
+// when the tile needs a mask, or when, in some row, the tile's largest p is more than this
+// share of the row's mass so far (its running sum plus that p).  So every key that keeps one
+// E4M3 term holds at most this share of its row's final sum, and the single-term rounding
+// (up to 2^-4 relative per weight) stays spread over many keys.
+constexpr float kTwoTermShare = 0.125f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -160,7 +166,7 @@ struct Cfg {
     static constexpr int Q_BYTES = kTileM * D;
     static constexpr int K_BYTES = kTileN * D;
     static constexpr int V_BYTES = kTileN * DV;
-    static constexpr int MISC_BYTES = 6144;
+    static constexpr int MISC_BYTES = 6208;
     static constexpr int SMEM_LIMIT = 232448;  // max dynamic smem per block on sm_103
     static constexpr int STAGES_FIT =
         (SMEM_LIMIT - 1024 - MISC_BYTES - kTraceSmemBytes - Q_BYTES) / (K_BYTES + V_BYTES);
@@ -544,6 +550,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     float *row_scale = reinterpret_cast<float *>(misc + 3072);   // [128]
     float *mx_part = reinterpret_cast<float *>(misc + 3584);     // [2 parity][2 half][128]
     float *sum_part = reinterpret_cast<float *>(misc + 5632);    // [128]
+    int *two_term_votes = reinterpret_cast<int *>(misc + 6144);   // [NS][8 softmax warps]
     const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
     const uint32_t sK = ptx::smem_u32(smem + C::OFF_K);
     const uint32_t sV = ptx::smem_u32(smem + C::OFF_V);
@@ -697,8 +704,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (!W.wait_warp(BAR(C::B_VF + vs), (uint32_t)(j / C::STAGES) & 1u)) return false;
             FA8_EV(11, j);
             ptx::tc_fence_after();
+            // two-term P: every softmax warp wrote its vote before arriving on B_PF
+            const volatile int *votes = two_term_votes + sb * 8;
             const bool two_term = tile_needs_mask((t_beg + j) * kTileN, Lk, p.causal, p.window_left, pos0,
-                                                  pos_last, delta);
+                                                  pos_last, delta) ||
+                                  (votes[0] | votes[1] | votes[2] | votes[3] | votes[4] | votes[5] | votes[6] |
+                                   votes[7]) != 0;
             const uint64_t dv_stage = dv0 + (uint64_t)((vs * C::V_BYTES) >> 4);
             const uint32_t s_col = tmem + C::TM_S + sb * 128;
 #pragma unroll
@@ -814,12 +825,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             const float mx = fmaxf(mh, mx_part[((it & 1) * 2 + (h ^ 1)) * 128 + r]);
             if (tid == 0) FA8_EV(1, it);
             float alpha = 1.f;
+            bool two_term = need_mask;
             if (warp_active) {
                 const float mt = mx * c;
                 if (mt > m_run + kTau) {
                     alpha = ptx::ex2(m_run - mt);
                     row_sum *= alpha;
                     m_run = mt;
+                }
+                if (!need_mask) {
+                    // a dominant key: the tile's largest p against this half's mass so far (at
+                    // most the row's, so the vote errs towards two terms)
+                    const float pm = ptx::ex2(mt - m_run + kPBias);
+                    two_term = __any_sync(0xffffffffu, row_ok && pm > kTwoTermShare * (row_sum + pm));
                 }
                 // p = 2^(s c - m) in f16 (MUFU, two values per instruction; the argument is
                 // near 0 where p is large, so f16 keeps it to 2^-11), P = e4m3(2^8 p) with the
@@ -858,7 +876,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         u[g][2 * k + 1] = q23;
                     }
                     ptx::tmem_st8(scol + 32 * g, w);
-                    if (need_mask) {
+                    if (two_term) {
                         // second E4M3 term on masked tiles: P_lo = e4m3(2^8 p - P_hi), in f16
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
@@ -866,6 +884,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             const uint32_t d23 = ptx::hsub2(u[g][2 * k + 1], ptx::e4m3x2_to_h2(w[k] >> 16));
                             w[k] = ptx::cvt_e4m3x2_h2(d01) | (ptx::cvt_e4m3x2_h2(d23) << 16);
                         }
+                        ptx::tmem_st8(scol + 32 * g + 8, w);
+                    } else {
+                        // another warp may vote for two terms: this warp's second term is zero
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) w[k] = 0u;
                         ptx::tmem_st8(scol + 32 * g + 8, w);
                     }
                 }
@@ -876,6 +899,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 // the f16 p carry no 2^8 factor: scale the tile's sum to the biased row sum
                 row_sum += (a0 + a1) * 256.f;
             }
+            if (lane == 0) two_term_votes[sb * 8 + warp] = two_term ? 1 : 0;
             ptx::tc_fence_before();
             ptx::mbar_arrive(BAR(C::B_PF + sb));
             if (tid == 0) FA8_EV(5, it);

@@ -118,6 +118,16 @@ def _raise(st: int):
         raise Fa8Error(st, lib().fa8_last_error().decode())
 
 
+def _on_device(device):
+    """Makes ``device`` current for the library call: the library plans for, and looks up its
+    per-device state on, the current CUDA device."""
+    import contextlib
+
+    if device.type != "cuda":
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 def _stream_handle(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
@@ -131,8 +141,9 @@ def plan(q, k, v, *, cu_seqlens_q=None, cu_seqlens_k=None, block_table=None, pag
     splits = ctypes.c_int(0)
     nbytes = ctypes.c_size_t(0)
     if sm_count is None:
-        st = lib().fa8_fwd_workspace_size(*[_ref(x) for x in views], int(page_size), int(num_splits),
-                                          ctypes.byref(splits), ctypes.byref(nbytes))
+        with _on_device(q.device):
+            st = lib().fa8_fwd_workspace_size(*[_ref(x) for x in views], int(page_size), int(num_splits),
+                                              ctypes.byref(splits), ctypes.byref(nbytes))
         _raise(st)
         return splits.value, nbytes.value, None
     grid = (ctypes.c_int64 * 2)()
@@ -165,17 +176,18 @@ def fwd(q, k, v, *, descale_q=None, descale_k=None, descale_v=None, out=None, ls
                  ck=_view(cu_seqlens_k), bt=_view(block_table), sink=_view(sink))
     ws_ptr = ctypes.c_void_p(workspace.data_ptr() if workspace is not None else 0)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib().fa8_fwd(_ref(views["q"]), _ref(views["k"]), _ref(views["v"]), _ref(views["dq"]),
-                       _ref(views["dk"]), _ref(views["dv"]), _ref(views["out"]), _ref(views["lse"]),
-                       _ref(views["cq"]), _ref(views["ck"]), _ref(views["bt"]), int(page_size),
-                       int(bool(causal)), int(window_left), _ref(views["sink"]), float(softmax_scale),
-                       int(num_splits), ws_ptr, ws_bytes,
-                       _stream_handle(stream, dev) if dev.type == "cuda" else ctypes.c_void_p(0))
+    with _on_device(dev):
+        st = lib().fa8_fwd(_ref(views["q"]), _ref(views["k"]), _ref(views["v"]), _ref(views["dq"]),
+                           _ref(views["dk"]), _ref(views["dv"]), _ref(views["out"]), _ref(views["lse"]),
+                           _ref(views["cq"]), _ref(views["ck"]), _ref(views["bt"]), int(page_size),
+                           int(bool(causal)), int(window_left), _ref(views["sink"]), float(softmax_scale),
+                           int(num_splits), ws_ptr, ws_bytes,
+                           _stream_handle(stream, dev) if dev.type == "cuda" else ctypes.c_void_p(0))
     _raise(st)
     return out, lse
 
 
-STATIC_SCRATCH_BYTES = 32 * 1024 * 1024  # FA8_STATIC_SCRATCH_BYTES
+STATIC_SCRATCH_BYTES = 32 * 1024 * 1024  # FA8_STATIC_SCRATCH_BYTES in include/fa8.h (a CPU test compares them)
 
 
 def fwd_static_scratch(q, k, v, *, out, lse=None, descale_q=None, descale_k=None, descale_v=None,
@@ -186,12 +198,13 @@ def fwd_static_scratch(q, k, v, *, out, lse=None, descale_q=None, descale_k=None
     views = dict(q=_view(q), k=_view(k), v=_view(v), dq=_view(descale_q), dk=_view(descale_k),
                  dv=_view(descale_v), out=_view(out), lse=_view(lse), cq=_view(cu_seqlens_q),
                  ck=_view(cu_seqlens_k), bt=_view(block_table), sink=_view(sink))
-    st = lib().fa8_fwd_static_scratch(_ref(views["q"]), _ref(views["k"]), _ref(views["v"]), _ref(views["dq"]),
-                                      _ref(views["dk"]), _ref(views["dv"]), _ref(views["out"]),
-                                      _ref(views["lse"]), _ref(views["cq"]), _ref(views["ck"]),
-                                      _ref(views["bt"]), int(page_size), int(bool(causal)), int(window_left),
-                                      _ref(views["sink"]), float(softmax_scale), int(num_splits),
-                                      _stream_handle(stream, q.device))
+    with _on_device(q.device):
+        st = lib().fa8_fwd_static_scratch(_ref(views["q"]), _ref(views["k"]), _ref(views["v"]),
+                                          _ref(views["dq"]), _ref(views["dk"]), _ref(views["dv"]),
+                                          _ref(views["out"]), _ref(views["lse"]), _ref(views["cq"]),
+                                          _ref(views["ck"]), _ref(views["bt"]), int(page_size), int(bool(causal)),
+                                          int(window_left), _ref(views["sink"]), float(softmax_scale),
+                                          int(num_splits), _stream_handle(stream, q.device))
     _raise(st)
     return out, lse
 

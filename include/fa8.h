@@ -185,9 +185,17 @@ FA8_API fa8_status fa8_fwd_static_scratch(const fa8_tensor *q, const fa8_tensor 
                                           float softmax_scale, int num_splits, void *stream);
 
 /*
- * fa8_check -- synchronises `stream`, then reads and clears the library's device status
- * word for the current device: FA8_SUCCESS, FA8_ERR_DEVICE_TIMEOUT (a kernel gave up a
- * bounded wait and returned early; its outputs are undefined) or FA8_ERR_DEVICE_BOUNDS.
+ * fa8_check -- reads the library's device status word of the current device on `stream`
+ * (ordered after the work enqueued there), waits for that read, and clears the word if it
+ * was set: FA8_SUCCESS, FA8_ERR_DEVICE_TIMEOUT (a kernel gave up a bounded wait and
+ * returned early; its outputs are undefined) or FA8_ERR_DEVICE_BOUNDS.
+ *
+ * The status word is one per device, shared by every stream and host thread that calls the
+ * library on that device: a kernel on any stream sets its bits, and a check on any stream
+ * reads and clears them all.  So a check may report (and clear) an error raised by another
+ * stream's work, and work still running on another stream may set the word after the read.
+ * Callers that run forwards on several streams at once and need to know which call failed
+ * should check from one place after joining the streams.
  */
 FA8_API fa8_status fa8_check(void *stream);
 
@@ -196,15 +204,17 @@ FA8_API fa8_status fa8_check(void *stream);
  * per kv-head (Sq x Hq/Hkv <= 16, Hq/Hkv dividing 16, dv a multiple of 128) run the decode
  * kernel, which puts the keys of a tile on the MMA's M dimension and the few query rows on
  * N; 0: every shape runs the 128-row forward kernel.  Both compute the same attention (not
- * bit-identically).  A process-wide setting read at each fa8_fwd call.
+ * bit-identically).  A process-wide setting, safe to change from any host thread: each
+ * fa8_fwd call reads it once, so one call uses one setting throughout.
  */
 FA8_API fa8_status fa8_set_decode_kernel(int enable);
 
-/* Sets the bound on every in-kernel wait (nanoseconds; default 2e9, minimum 1e5). */
+/* Sets the bound on every in-kernel wait (nanoseconds; default 2e9, minimum 1e5); a
+ * process-wide setting, read once by each later fa8_fwd call, safe from any host thread. */
 FA8_API fa8_status fa8_set_wait_timeout_ns(uint64_t ns);
 
 /*
- * fa8_debug_wait_probe -- launches a one-CTA kernel whose only work is a bounded wait on a
+ * fa8_debug_wait_probe -- DEBUG ONLY.  Launches a one-CTA kernel whose only work is a bounded wait on a
  * barrier that nothing completes, then returns fa8_check(stream).  It exists to test the
  * timeout path: with the default bound it returns FA8_ERR_DEVICE_TIMEOUT after ~2 s.
  */
@@ -215,7 +225,8 @@ FA8_API fa8_status fa8_debug_wait_probe(void *stream);
  * record clock64() at each pipeline event (TMA issue, MMA issue, softmax and fold
  * hand-offs) of the first 8 CTAs into `device_buffer`, laid out [cta 8][event 16][tile 64]
  * as uint64 (needs 65536 bytes); NULL turns it off.  Other builds return
- * FA8_ERR_UNSUPPORTED.  Intended for pipeline tuning, not for production use.
+ * FA8_ERR_UNSUPPORTED.  DEBUG ONLY: for pipeline tuning with a trace build; production
+ * builds do not record anything.
  */
 FA8_API fa8_status fa8_debug_set_trace_buffer(void *device_buffer, size_t bytes);
 

@@ -90,6 +90,19 @@ typedef struct {
     const int32_t *rows_head;
 } oracle_problem;
 
+#if ORACLE_MUTANT == 10
+/* a + b rounded to fp32 toward zero (exact sum in fp64, then the fp32 neighbour of
+   smaller magnitude) */
+static float truncf_add(float a, float b)
+{
+    double e = (double)a + (double)b;
+    float f = (float)e;
+    if (fabs((double)f) > fabs(e))
+        f = nextafterf(f, 0.0f);
+    return f;
+}
+#endif
+
 /* Pointer to key row j (0-based within request b) for kv-head g. */
 static const uint8_t *key_row(const oracle_problem *p, const uint8_t *base, int width,
                               int b, int g, int64_t j)
@@ -182,8 +195,15 @@ static void one_row(const oracle_problem *p, int b, int64_t tok, int h, double *
         double w = exp(s[j] - m);
         Z += w;
         const uint8_t *vrow = key_row(p, p->v, p->DV, b, g, j);
-        for (int c = 0; c < p->DV; ++c)
+        for (int c = 0; c < p->DV; ++c) {
+#if ORACLE_MUTANT == 10
+            /* O accumulated in fp32 with every add truncated toward zero: a reduced-precision
+               accumulator whose rounding loss grows with the key count */
+            o_row[c] = truncf_add((float)o_row[c], (float)(w * oracle_e4m3_decode(vrow[c])));
+#else
             o_row[c] += w * oracle_e4m3_decode(vrow[c]);
+#endif
+        }
     }
 #if ORACLE_MUTANT == 6
     (void)sk; /* sink dropped from the denominator */

@@ -93,6 +93,21 @@ def run_gpu(case, **kw):
     return out, lse
 
 
+# Every parity check made in this process: (test, case, rows checked, max, mean, LSE error,
+# and the bars), printed by the test session's summary and written to FA8_PARITY_LOG when set.
+MARGINS = []
+
+
+def record_margin(case_cpu, mx, mean, le, rows=None, extra=""):
+    import os
+
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    MARGINS.append({"test": test, "case": case_cpu.name + (f" {extra}" if extra else ""),
+                    "rows": "all" if rows is None else len(rows), "max_abs": mx, "mean_abs": mean,
+                    "lse_abs": le, "bars": [MAX_ABS, MEAN_ABS, LSE_ABS],
+                    "ok": bool(mx <= MAX_ABS and mean <= MEAN_ABS and le <= LSE_ABS)})
+
+
 def assert_parity(case_cpu, rows=None, device="cuda", **kw):
     """Runs the case on the GPU and the oracle (all rows or `rows`) and checks tolerances."""
     c = case_cpu.to(device)
@@ -100,6 +115,7 @@ def assert_parity(case_cpu, rows=None, device="cuda", **kw):
     o, l = gpu_outputs(case_cpu, out, lse)
     o_ref, l_ref = oracle.attention(case_cpu, rows=rows)
     mx, mean, le = errors(case_cpu, o, l, o_ref, l_ref, rows=rows)
+    record_margin(case_cpu, mx, mean, le, rows)
     assert mx <= MAX_ABS and mean <= MEAN_ABS and le <= LSE_ABS, (
         f"{case_cpu.name}: max {mx:.3g} mean {mean:.3g} lse {le:.3g}")
     return mx, mean, le, out, lse

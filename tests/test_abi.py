@@ -218,3 +218,54 @@ def test_decode_step_shapes_use_the_decode_kernel(lib):
         cu = torch.zeros((reqs + 1,), dtype=torch.int32)
         s, _, grid = plan(q, kp, kp, cu_seqlens_k=cu, block_table=bt, page_size=ps, num_splits=1)
         assert s == 1 and grid == (reqs, hkv), name
+
+
+def test_static_scratch_size_matches_the_header():
+    """The binding's size limit for fa8_fwd_static_scratch is the header's."""
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+FA8_STATIC_SCRATCH_BYTES\s+\(\(size_t\)\s*(\d+)\s*\*\s*(\d+)\s*\*\s*(\d+)\)", text)
+    assert m, "FA8_STATIC_SCRATCH_BYTES not found in include/fa8.h"
+    a, b, c = (int(x) for x in m.groups())
+    assert a * b * c == fa8.STATIC_SCRATCH_BYTES
+
+
+def test_settings_from_many_threads_keep_plans_consistent(lib):
+    """fa8_set_decode_kernel and fa8_set_wait_timeout_ns are process-wide and may be called
+    from any host thread while others plan: every plan is one of the two valid ones (decode
+    kernel on: up to 128 splits; off: the 128-row kernel's 64), never a mix."""
+    import threading
+
+    q, k, v = qkv(B=8, Sq=1, Sk=32768, Hq=16, Hkv=2)
+    # the split heuristic caps the decode kernel at 128 splits, the 128-row kernel at 64
+    on = fa8.plan(q, k, v, sm_count=152, num_splits=0)
+    fa8.set_decode_kernel(False)
+    off = fa8.plan(q, k, v, sm_count=152, num_splits=0)
+    fa8.set_decode_kernel(True)
+    assert on != off
+    bad, stop = [], threading.Event()
+
+    def toggler(i):
+        n = 0
+        while not stop.is_set():
+            fa8.set_decode_kernel(n % 2 == 0)
+            lib.fa8_set_wait_timeout_ns(1_000_000 + 1000 * i + n)
+            n += 1
+
+    def planner():
+        for _ in range(300):
+            got = fa8.plan(q, k, v, sm_count=152, num_splits=0)
+            if got not in (on, off):
+                bad.append(got)
+
+    ts = [threading.Thread(target=toggler, args=(i,)) for i in range(2)]
+    ps = [threading.Thread(target=planner) for _ in range(4)]
+    for t in ts + ps:
+        t.start()
+    for t in ps:
+        t.join()
+    stop.set()
+    for t in ts:
+        t.join()
+    fa8.set_decode_kernel(True)
+    assert lib.fa8_set_wait_timeout_ns(2_000_000_000) == fa8.FA8_SUCCESS
+    assert not bad, bad[:3]

@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from fp8_attention_forward_gb300 import build, fa8, inputs
-from parity_util import (LSE_ABS, MAX_ABS, MEAN_ABS, assert_parity, errors, gpu_outputs,
+from parity_util import (LSE_ABS, MAX_ABS, MEAN_ABS, assert_parity, errors, gpu_outputs, record_margin,
                          run_gpu, sample_rows)
 
 pytestmark = pytest.mark.gpu
@@ -185,6 +185,24 @@ def test_paged_bit_exact_vs_contiguous(ps):
     assert torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("splits", [1, 3], ids=["one_split", "three_splits"])
+@pytest.mark.parametrize("ps", [16, 64, 128])
+def test_rows128_paged_bit_exact_vs_contiguous(ps, splits):
+    """The 128-row kernel (prefill, chunked prefill: more than 16 query rows per kv-head)
+    reads paged K/V as page-aligned boxes and contiguous K/V as whole tiles; both land the
+    same bytes in the same shared-memory tiles, so O and LSE must be bit-identical, with
+    one split and with three."""
+    case = inputs.make_case(name="pg128", B=2, Hq=8, Hkv=2, D=128, DV=128, seqlens_q=[200, 333],
+                            seqlens_k=[600, 333], q_layout="varlen", kv_layout="paged", page_size=ps,
+                            causal=True, sink=True, descale_mode="per_bkv_uniform", seed=143)
+    assert max(case.seqlens_q) * case.Hq // case.Hkv > 16  # the 128-row kernel
+    contig = _paged_to_contig(case)
+    o1, l1 = run_gpu(case.to("cuda"), num_splits=splits)
+    o2, l2 = run_gpu(contig.to("cuda"), num_splits=splits)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
 def test_split_path_bit_exact_when_one_split_has_keys():
     """Every request fits one 128-key tile: with 4 splits only split 0 has keys, and the
     combine must reproduce the direct path bit for bit (sink included)."""
@@ -226,6 +244,7 @@ def _full(case_fn, n_rows=48, **kw):
     o, l = gpu_outputs(cpu_case, out, lse)
     o_ref, l_ref = oracle.attention(cpu_case, rows=rows)
     mx, mean, le = errors(cpu_case, o, l, o_ref, l_ref, rows=rows)
+    record_margin(cpu_case, mx, mean, le, rows, extra="full size, sampled rows")
     assert mx <= MAX_ABS and mean <= MEAN_ABS and le <= LSE_ABS, (case.name, mx, mean, le)
     return out, lse
 

@@ -10,7 +10,7 @@ The oracle is only trusted after it agrees with things other than itself:
     paged == gathered contiguous, linearity in the V descale, dq/dk symmetry;
   * the nonzero-mean V property at long key lengths.
 ``test_planted_mistakes_are_caught`` compiles the oracle with each planted mistake
-(ORACLE_MUTANT=1..9) and checks that at least one of these pins fails for it.
+(ORACLE_MUTANT=1..10) and checks that at least one of these pins fails for it.
 """
 import math
 import os
@@ -347,12 +347,18 @@ def pin_descale_structure(mutant):
 
 
 def pin_nonzero_mean_v(mutant):
-    """V ~ N(1, 0.1): the softmax-weighted mean of V stays near 1 at 20k keys."""
-    case = inputs.make_case(B=1, Hq=2, Hkv=1, D=64, DV=32, seqlens_q=[1], seqlens_k=[20000],
+    """V ~ N(1, 0.1) independent of the scores, 131072 keys (the long-KV length): the
+    softmax-weighted mean of V equals the plain mean of the dequantised V up to sampling
+    noise (std ~1e-4 here: 0.1 / sqrt(effective key count ~5e4), averaged over 64 columns).
+    A reduced-precision O accumulator that loses a little of every add shrinks it by far more
+    ("[Cute,Fwd,Sm90] Native FP8 (E4M3 Q/K/V) forward for Hopper", Design, "Two-level PV
+    accumulation": the output shrinks with the key count when the accumulator truncates)."""
+    case = inputs.make_case(B=1, Hq=2, Hkv=1, D=64, DV=32, seqlens_q=[1], seqlens_k=[131072],
                             v_dist=(1.0, 0.1), descale_mode="tensor_amax", seed=32)
     o, _ = oracle.attention(case, mutant=mutant)
     dv = float(case.descale_v)
-    return abs(float(o.mean()) / dv * dv - 1.0) < 0.02
+    v_mean = float(case.v.float().double().mean()) * dv
+    return abs(float(o.mean()) - v_mean) < 1e-3 and abs(v_mean - 1.0) < 0.02
 
 
 def pin_split_merge(mutant):
@@ -411,7 +417,7 @@ def test_empty_rows(oracle_lib):
     assert np.all(o2[:4] == 0) and np.allclose(l2[:4], [[0.25, -1.0]] * 4, atol=0, rtol=0)
 
 
-N_MUTANTS = 9
+N_MUTANTS = 10
 
 
 @pytest.mark.parametrize("mutant", range(1, N_MUTANTS + 1))
