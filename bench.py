@@ -40,8 +40,8 @@ METRIC = "FP8 attn fwd TFLOP/s (prefill) & decode HBM GB/s; % of GB300 roofline"
 # DRAM bytes (read + write) per launch from one ncu capture of each timed kernel (summaries
 # under profiles/), valid only while the kernel sources hash to the value recorded with it.
 PROFILED_TRAFFIC = {
-    "prefill": {"kernel": "fwd_kernel<128,128>", "bytes": 68.41e6,
-                "sources": ["fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "92e86360ee36f6f1"},
+    "prefill": {"kernel": "prefill_kernel<128,128>", "bytes": 68.41e6,
+                "sources": ["fa8_prefill.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "0000000000000000"},
     "decode": {"kernel": "decode_kernel<128,128>", "bytes": 2073.6e6,
                "sources": ["fa8_decode.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "a855ada72c561ba6"},
 }
@@ -189,9 +189,11 @@ def bench_case(case, steps, warmup, flush, fa8, num_splits=0, graph=False):
     launches = 1
     if splits > 1:
         sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-        per_sm = 2 if _decode_kernel_name(case).startswith("decode_kernel<128,128>") else 1
+        name = _decode_kernel_name(case)
+        per_sm = 2 if name.startswith("decode_kernel<128,128>") else 1
         g = case.Hq // case.Hkv
-        pos = (16 if _decode_kernel_name(case).startswith("decode_kernel") else 128) // g  # positions per tile
+        # positions per CTA: a 16-row decode tile, two 128-row tiles (prefill), or one
+        pos = 16 // g if name.startswith("decode_kernel") else (2 if name.startswith("prefill") else 1) * (128 // g)
         mblocks = sum((lq + pos - 1) // pos for lq in case.seqlens_q)
         base = mblocks * case.Hkv
         launches = 2 + (1 if base * splits > per_sm * sms else 0)
@@ -324,11 +326,14 @@ def cpu_oracle_sample(case, budget_s=15.0, seed=0):
 
 def _decode_kernel_name(case):
     """The kernel include/fa8.h documents for this shape: the few-rows decode kernel when
-    query positions x (Hq / Hkv) <= 16 with Hq / Hkv dividing 16 (batched q, dv % 128 = 0)."""
+    query positions x (Hq / Hkv) <= 16 with Hq / Hkv dividing 16 (batched q, dv % 128 = 0);
+    otherwise the two-tile prefill kernel for dv <= 128 and the one-tile kernel above."""
     g = case.Hq // case.Hkv
     sq = case.seqlens_q[0]
     few = case.q_layout == "batched" and case.DV % 128 == 0 and 16 % g == 0 and sq * g <= 16
-    return f"decode_kernel<{case.D},{case.DV}>" if few else f"fwd_kernel<{case.D},{case.DV}>"
+    if few:
+        return f"decode_kernel<{case.D},{case.DV}>"
+    return f"prefill_kernel<{case.D},{case.DV}>" if case.DV <= 128 else f"fwd_kernel<{case.D},{case.DV}>"
 
 
 def decode_steps_suite(args):

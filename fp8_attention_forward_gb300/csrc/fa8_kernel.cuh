@@ -81,10 +81,19 @@ constexpr int kTraceSmemBytes = kTraceEvents * kTraceTiles * 8;
         if ((it) < kTraceTiles)                                                         \
             reinterpret_cast<unsigned long long *>(smem + C::OFF_TRACE)[(ev) * kTraceTiles + (it)] = clock64(); \
     } while (0)
+// records a value instead of a clock
+#define FA8_VAL(ev, it, v)                                                              \
+    do {                                                                                \
+        if ((it) < kTraceTiles)                                                         \
+            reinterpret_cast<unsigned long long *>(smem + C::OFF_TRACE)[(ev) * kTraceTiles + (it)] = (v); \
+    } while (0)
 #else
 constexpr int kTraceSmemBytes = 0;
 #define FA8_EV(ev, it) \
     do {               \
+    } while (0)
+#define FA8_VAL(ev, it, v) \
+    do {                   \
     } while (0)
 #endif
 
@@ -240,6 +249,27 @@ __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatil
         if (*abort) return false;
         if (ptx::globaltimer() - t0 > timeout) {
             *abort = 1;
+            atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+// As Waiter::wait_warp, for roles that keep as few registers as possible live: the abort flag by
+// its shared-memory address, the bound and status word read from the kernel parameters only
+// on the slow path.
+__device__ __forceinline__ bool wait_slow_s(uint32_t bar, uint32_t parity, uint32_t abort_saddr,
+                                            unsigned long long timeout, unsigned int *status) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+        int ab;
+        asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(ab) : "r"(abort_saddr));
+        if (ab) return false;
+        if (ptx::globaltimer() - t0 > timeout) {
+            asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(abort_saddr), "r"(1));
             atomicOr(status, kStatusTimeout);
             return false;
         }

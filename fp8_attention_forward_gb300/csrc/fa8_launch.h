@@ -7,6 +7,7 @@
 
 #include "fa8_decode.cuh"
 #include "fa8_kernel.cuh"
+#include "fa8_prefill.cuh"
 
 namespace fa8 {
 
@@ -16,6 +17,10 @@ cudaError_t launch_fwd(const FwdParams &p, const CUtensorMap &tq, const CUtensor
 
 template <int DV>
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+
+template <int D, int DV>
+cudaError_t launch_prefill(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                           const CUtensorMap &tv, dim3 grid, cudaStream_t stream);
 
 // CTAs of decode_kernel<D, DV> resident per SM (shared memory decides).
 inline int decode_ctas_per_sm(int D, int DV) {
@@ -83,6 +88,23 @@ inline cudaError_t launch_after_plan(K *kernel, const FwdParams &p, const CUtens
                                  smem);                                                      \
         if (e != cudaSuccess) return e;                                                      \
         return launch_after_plan(fwd_kernel<D_, DV_>, p, tq, tk, tv, grid, kNumThreads, smem, stream); \
+    }
+
+// Defines launch_prefill<D, DV> (two 128-row Q tiles per CTA, dv <= 128); like
+// fwd_kernel it re-balances registers with setmaxnreg and checks the compiled count.
+#define FA8_DEFINE_PREFILL(D_, DV_)                                                          \
+    template <>                                                                              \
+    cudaError_t launch_prefill<D_, DV_>(const FwdParams &p, const CUtensorMap &tq,           \
+                                        const CUtensorMap &tk, const CUtensorMap &tv,        \
+                                        dim3 grid, cudaStream_t stream) {                    \
+        constexpr int smem = PfCfg<D_, DV_>::SMEM_BYTES;                                     \
+        static int regs = -1;                                                                \
+        cudaError_t e = check_launch_regs(prefill_kernel<D_, DV_>, kPfLaunchRegs, &regs);    \
+        if (e != cudaSuccess) return e;                                                      \
+        e = cudaFuncSetAttribute(prefill_kernel<D_, DV_>,                                    \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);         \
+        if (e != cudaSuccess) return e;                                                      \
+        return launch_after_plan(prefill_kernel<D_, DV_>, p, tq, tk, tv, grid, kPfThreads, smem, stream); \
     }
 
 // Defines launch_decode<D, DV> (the few-rows kernel, dv a multiple of 128).
