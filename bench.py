@@ -3,7 +3,9 @@
 Headline: causal GQA prefill (B=2, Hq=32, Hkv=8, S=4096, d=dv=128, E4M3 in, bf16 out) in
 TFLOP/s of algorithmic work (2*(d+dv) flops per unmasked (row, key) pair), against the
 dense FP8 tensor peak.  The same line carries the paged decode workload (B=64, 1 token,
-Hq=64, Hkv=8, d=dv=128, 16-token pages, keys ~U[1024,32768]) in GB/s against HBM.
+Hq=64, Hkv=8, d=dv=128, 16-token pages, keys ~U[1024,32768]) in GB/s against HBM, every
+configured workload on its own roofline (`configs`), and the fp64 oracle's throughput on
+each workload at one host thread and at all host threads (`cpu_baseline`).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -13,8 +15,11 @@ stream; ms_per_step is the mean over the K steps, max over ranks.  `e2e` repeats
 measurement through the public call with the inputs copied from pinned host memory and
 the output copied back inside the timed region (pipelined over two buffer sets so that the
 copies of neighbouring steps overlap the forward; the serial time is reported beside it).
-`--impl reference` times the fp64 CPU oracle (the only reference this path has) on a
-bounded sample of the same workload.
+`--impl reference` times the fp64 CPU oracle (the only reference this path has) on the same
+workload: W warm-up and K timed steps, each a bounded sample of rows on all host cores.
+Tensor-bound fractions also come as `frac_at_run_clock`: the measured peak was taken at a
+lower SM clock (its median under load) than this run's, so the same work at this run's clock
+is compared with the peak scaled to that clock.
 """
 from __future__ import annotations
 
@@ -289,39 +294,73 @@ def bench_e2e(case, steps, warmup, flush, fa8, num_splits=0):
     return {"ms": ms, "ms_serial": ser, "h2d": h2d, "d2h": d2h}
 
 
-def cpu_oracle_sample(case, budget_s=15.0, seed=0):
-    """Times the fp64 oracle (single thread) on randomly sampled output rows of `case`
-    until ~budget_s of CPU work; returns (flop/s, rows, seconds)."""
+def _row_pairs(case, rows):
+    """Visible (row, key) pairs of the sampled (token, head) rows."""
+    import numpy as np
+
+    starts = np.concatenate([[0], np.cumsum(case.seqlens_q)])
+    n = 0
+    for tok, _ in rows:
+        b = int(np.searchsorted(starts, tok, side="right") - 1)
+        i = tok - starts[b]
+        lq, lk = case.seqlens_q[b], case.seqlens_k[b]
+        hi = lk - 1
+        if case.causal:
+            hi = min(hi, i + lk - lq)
+        lo = 0 if case.window_left < 0 else max(0, i + lk - lq - case.window_left)
+        n += max(0, hi - lo + 1)
+    return n
+
+
+def cpu_oracle_sample(case, budget_s=15.0, seed=0, threads=1, arrays=None):
+    """Times the fp64 oracle on randomly sampled output rows of `case` until ~budget_s of
+    wall time, with `threads` host threads working on independent rows (the C oracle runs
+    without the interpreter lock); returns (pairs per second, rows, seconds).  The
+    whole-workload time is the sampled time scaled by the workload's visible pairs."""
+    import concurrent.futures as cf
+
     import numpy as np
 
     import oracle
 
-    arrays = oracle.problem_arrays(case)
+    a = arrays if arrays is not None else oracle.problem_arrays(case)
     rng = np.random.default_rng(seed)
-    total_flops = 0.0
+    per_call = 4
+    pairs = 0
     rows_done = 0
     t0 = time.perf_counter()
-    lens_q = case.seqlens_q
-    lens_k = case.seqlens_k
-    starts = np.concatenate([[0], np.cumsum(lens_q)])
-    while time.perf_counter() - t0 < budget_s:
-        rows = []
-        for _ in range(8):
-            tok = int(rng.integers(0, case.total_q))
-            rows.append((tok, int(rng.integers(0, case.Hq))))
-        oracle.attention_arrays(arrays, rows=rows)
-        for tok, _ in rows:
-            b = int(np.searchsorted(starts, tok, side="right") - 1)
-            i = tok - starts[b]
-            lq, lk = lens_q[b], lens_k[b]
-            hi = lk - 1
-            if case.causal:
-                hi = min(hi, i + lk - lq)
-            lo = 0 if case.window_left < 0 else max(0, i + lk - lq - case.window_left)
-            total_flops += 2.0 * (case.D + case.DV) * max(0, hi - lo + 1)
-        rows_done += len(rows)
+    with cf.ThreadPoolExecutor(threads) as ex:
+        while time.perf_counter() - t0 < budget_s:
+            batches = [[(int(rng.integers(0, case.total_q)), int(rng.integers(0, case.Hq))) for _ in range(per_call)]
+                       for _ in range(threads)]
+            list(ex.map(lambda r: oracle.attention_arrays(a, rows=r), batches))
+            for r in batches:
+                pairs += _row_pairs(case, r)
+                rows_done += len(r)
     dt = time.perf_counter() - t0
-    return total_flops / dt, rows_done, dt
+    return pairs / dt, rows_done, dt
+
+
+def cpu_baseline_for(case, bound, budget_s, threads):
+    """The oracle's throughput on `case` in the workload's own unit (TFLOP/s or GB/s of the
+    same algorithmic work the GPU figure counts), at one thread and at `threads` threads."""
+    import oracle
+
+    a = oracle.problem_arrays(case)
+    out = {}
+    for n in (1, threads):
+        pps, rows, dt = cpu_oracle_sample(case, budget_s=budget_s, threads=n, arrays=a)
+        t_full = case.pairs() / pps  # seconds for the whole workload at this rate
+        if bound == "hbm":
+            val, unit = inputs.algorithmic_bytes(case) / t_full / 1e9, "GB/s"
+        else:
+            val, unit = inputs.algorithmic_flops(case) / t_full / 1e12, "TFLOP/s"
+        out["threads_1" if n == 1 else f"threads_{n}"] = {
+            "value": val, "unit": unit, "cores": n, "rows": rows, "seconds": round(dt, 2),
+            "whole_workload_s": t_full}
+        if n == threads:
+            break
+    return out
 
 
 def _decode_kernel_name(case):
@@ -363,35 +402,110 @@ def decode_steps_suite(args):
         del case, r, eager
 
 
+WORKLOADS = [
+    # (key, what, builder, bound): the five configured workloads; the tiny one is launch-bound
+    # and reported for completeness only
+    ("tiny_dense", "tiny dense (B=1, H=2, S=128, d=64)", lambda dev: inputs.tiny_dense().to(dev), "launch"),
+    ("causal_gqa_prefill", "causal GQA prefill (B=2, Hq=32, Hkv=8, S=4096, d=dv=128)",
+     lambda dev: inputs.causal_gqa_prefill("full", device=dev), "tensor"),
+    ("paged_decode", "paged decode (B=64, 1 token, Hq=64, Hkv=8, keys U[1024,32768], 16-token pages)",
+     lambda dev: inputs.paged_decode("full", device=dev), "hbm"),
+    ("long_kv_sq1", "long-KV, 1 query row (Sk=131072, d=dv=256)", lambda dev: inputs.long_kv(1, "full", device=dev), "hbm"),
+    ("long_kv_sq128", "long-KV, 128 query rows (Sk=131072, d=dv=256)",
+     lambda dev: inputs.long_kv(128, "full", device=dev), "tensor"),
+    ("varlen_swa_prefill", "varlen sliding-window prefill (16 seqs U[256,8192], d=192, dv=128, window 1024, sink)",
+     lambda dev: inputs.varlen_swa_prefill("full", device=dev), "tensor"),
+]
+
+
+def _peak_clock_mhz():
+    """The SM clock the measured peaks were taken at (their median under load), if recorded."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        c = d.get("clocks_under_load", {}).get("sm_mhz_median")
+        return float(c) if c else None
+    return None
+
+
+def workload_line(key, what, case, bound, r, peaks, clk_mhz):
+    """One workload's GPU figure against its roofline."""
+    sec = r["ms"] * 1e-3
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    d = {"workload": key, "what": what, "kernel": _decode_kernel_name(case), "us": r["ms"] * 1e3,
+         "us_min": r["ms_min"] * 1e3, "splits": r["splits"], "bound": bound}
+    if bound == "hbm":
+        val = inputs.algorithmic_bytes(case) / sec / 1e9
+        d.update(value=val, unit="GB/s", peak=peaks["hbm_gbs"], frac=val / peaks["hbm_gbs"],
+                 algorithmic_bytes=inputs.algorithmic_bytes(case))
+    else:
+        val = inputs.algorithmic_flops(case) / sec / 1e12
+        d.update(value=val, unit="TFLOP/s", algorithmic_flops=inputs.algorithmic_flops(case))
+        if bound == "tensor":
+            d.update(peak=fp8_peak, frac=val / fp8_peak)
+            pc = _peak_clock_mhz()
+            if pc and clk_mhz:
+                # the peak was measured at a lower clock under its own power draw: the same
+                # fraction at this run's clock
+                d["frac_at_run_clock"] = val / (fp8_peak * clk_mhz / pc)
+    return d
+
+
 def configs_suite(args):
     """Times the forward on every configured workload (L2 flushed before every step) and
-    prints one JSON line each with its roofline fraction: tensor-bound workloads in TFLOP/s
-    against the dense FP8 peak, HBM-bound ones in GB/s against the copy bandwidth."""
-    import torch
-
+    prints one JSON line each with its roofline fraction."""
     from fp8_attention_forward_gb300 import fa8
 
     peaks = _peaks()
-    fp8_peak = 2.0 * peaks["bf16_tflops"]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    work = [("causal GQA prefill", lambda: inputs.causal_gqa_prefill("full", device="cuda"), "tensor"),
-            ("paged decode", lambda: inputs.paged_decode("full", device="cuda"), "hbm"),
-            ("long-KV, 1 query row", lambda: inputs.long_kv(1, "full", device="cuda"), "hbm"),
-            ("long-KV, 128 query rows", lambda: inputs.long_kv(128, "full", device="cuda"), "tensor"),
-            ("varlen sliding-window prefill", lambda: inputs.varlen_swa_prefill("full", device="cuda"), "tensor")]
-    for name, make, bound in work:
-        case = make()
+    for key, what, make, bound in WORKLOADS:
+        case = make("cuda")
         r = bench_case(case, args.steps, args.warmup, flush, fa8)
-        sec = r["ms"] * 1e-3
-        if bound == "tensor":
-            val, unit, peak = inputs.algorithmic_flops(case) / sec / 1e12, "TFLOP/s", fp8_peak
-        else:
-            val, unit, peak = inputs.algorithmic_bytes(case) / sec / 1e9, "GB/s", peaks["hbm_gbs"]
-        print(json.dumps({"suite": "configs", "workload": case.name, "what": name, "us": r["ms"] * 1e3,
-                          "value": val, "unit": unit, "bound": bound, "peak": peak, "frac": val / peak,
-                          "splits": r["splits"], "steps": args.steps, "warmup": args.warmup,
-                          "l2": "256 MB buffer written before every step"}))
+        line = workload_line(key, what, case, bound, r, peaks, None)
+        line.update(suite="configs", steps=args.steps, warmup=args.warmup, l2="256 MB buffer written before every step")
+        print(json.dumps(line))
         del case, r
+
+
+def reference_arm(args, rank):
+    """The fp64 CPU oracle (the only reference this path has) on the headline workload:
+    W warm-up and K timed steps, each a bounded sample of output rows computed on all host
+    cores; the value is the sample's throughput scaled to the workload's algorithmic flops."""
+    if rank != 0:
+        return
+    import oracle
+
+    case = inputs.causal_gqa_prefill("full", device="cpu")
+    a = oracle.problem_arrays(case)
+    threads = os.cpu_count() or 1
+    step_s = min(5.0, max(0.5, args.cpu_budget / max(1, args.steps)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(case, budget_s=0.2, threads=threads, arrays=a)
+    rates, rows = [], 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        pps, nr, _ = cpu_oracle_sample(case, budget_s=step_s, threads=threads, arrays=a, seed=100 + i)
+        rates.append(pps)
+        rows += nr
+    wall = time.perf_counter() - t0
+    pps = statistics.mean(rates)
+    val = pps * 2.0 * (case.D + case.DV) / 1e12
+    t_full = case.pairs() / pps
+    sample = (f"{args.steps} steps of ~{step_s:.1f} s: {rows} random (token, head) rows of the workload on "
+              f"{threads} host threads (fp64, independent rows per thread)")
+    line = {"metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_full * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": HEADLINE, "impl": "fp64 CPU oracle (oracle/attn_ref.c)",
+                       "ms_per_step": "the whole workload at the sampled rate"},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line))
+
+
+HEADLINE = "causal_gqa_prefill B=2 Hq=32 Hkv=8 Sq=Sk=4096 d=dv=128 e4m3->bf16"
 
 
 def main():
@@ -401,7 +515,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="fa8", choices=["fa8", "reference"])
     ap.add_argument("--no-decode", action="store_true", help="skip the paged-decode figure")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload section")
+    ap.add_argument("--cpu-budget", type=float, default=20.0,
+                    help="seconds of oracle time: the reference arm's total; per workload and thread count "
+                         "in the default line, a tenth of it")
     ap.add_argument("--suite", default="", choices=["", "decode-steps", "configs"],
                     help="decode-steps: one JSON line per served-model decode step shape "
                          "(kernel time incl. the split combine); configs: one line per "
@@ -416,27 +533,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return reference_arm(args, rank)
     peaks = _peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops"]  # dense FP8 = 2x dense bf16 (nominal 4.5 vs 2.25 PF)
-    workload = "causal_gqa_prefill B=2 Hq=32 Hkv=8 Sq=Sk=4096 d=dv=128 e4m3->bf16"
-
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        case = inputs.causal_gqa_prefill("full", device="cpu")
-        flops, rows, dt = cpu_oracle_sample(case, budget_s=args.cpu_budget)
-        val = flops / 1e12
-        sample = f"{rows} random (token, head) rows of the workload, {dt:.1f} s single-thread fp64"
-        line = {"metric": METRIC, "value": val, "unit": "TFLOP/s",
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "f64", "data": "synthetic", "impl": "reference",
-                "config": {"workload": workload, "impl": "fp64 CPU oracle (oracle/attn_ref.c)"},
-                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                                 "sample": sample},
-                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
-        return
 
     if world > 1:
         torch.cuda.set_device(local)
@@ -487,33 +587,74 @@ def main():
                                "peak_source": peaks["source"] + " copy bandwidth"}}
         del dec, dres
 
+    # every configured workload, each on its own roofline (fewer steps: a bounded section)
+    configs = None
+    if not args.no_configs:
+        lines = []
+        csteps, cwarm = max(3, min(args.steps, 10)), max(3, min(args.warmup, 3))
+        with ClockSampler(local) as cclocks:
+            for key, what, make, bound in WORKLOADS:
+                case = make("cuda")
+                r = bench_case(case, csteps, cwarm, flush, fa8)
+                line = workload_line(key, what, case, bound, r, peaks, None)
+                line.update(steps=csteps, warmup=cwarm)
+                lines.append(line)
+                del case, r
+        cclk = cclocks.summary()
+        pc = _peak_clock_mhz()
+        for line in lines:
+            if line["bound"] == "tensor" and pc and cclk.get("sm_mhz"):
+                line["frac_at_run_clock"] = line["value"] / (line["peak"] * cclk["sm_mhz"] / pc)
+        configs = {"steps": csteps, "warmup": cwarm, "clocks": cclk, "l2": "256 MB buffer written before every step",
+                   "workloads": lines}
+
     cpu = None
     if rank == 0:
-        cpu_case = prefill.to("cpu")
-        cflops, crows, cdt = cpu_oracle_sample(cpu_case, budget_s=args.cpu_budget)
-        cpu = {"value": cflops / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-               "sample": f"{crows} random (token, head) rows of the prefill workload, {cdt:.1f} s, single-thread fp64"}
+        threads = os.cpu_count() or 1
+        budget = max(0.5, args.cpu_budget / 10.0)
+        per_config = {}
+        head = cpu_baseline_for(prefill.to("cpu"), "tensor", budget, threads)
+        per_config["causal_gqa_prefill"] = head
+        if configs is not None:
+            for key, what, make, bound in WORKLOADS:
+                if key in per_config:
+                    continue
+                ccase = make("cuda").to("cpu")  # drawn on the device (fast), read by the oracle on the host
+                per_config[key] = cpu_baseline_for(ccase, "hbm" if bound == "hbm" else "tensor", budget, threads)
+                del ccase
+        st = head["threads_1"]
+        cpu = {"value": st["value"], "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{st['rows']} random (token, head) rows of the prefill workload, {st['seconds']} s, "
+                         f"single-thread fp64, scaled to the workload's algorithmic flops",
+               "all_cores": head.get(f"threads_{threads}"), "host_threads": threads,
+               "per_config": per_config}
 
     if rank == 0:
+        pc = _peak_clock_mhz()
+        roof = {"bound": "tensor", "achieved": tflops_rank, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": tflops_rank / fp8_peak, "traffic": _profiled_traffic("prefill"),
+                "kernel": PROFILED_TRAFFIC["prefill"]["kernel"],
+                "peak_source": f"{peaks['source']} bf16 burst x2 (dense FP8 = 2x bf16)"}
+        if pc and clk.get("sm_mhz"):
+            roof["frac_at_run_clock"] = tflops_rank / (fp8_peak * clk["sm_mhz"] / pc)
+            roof["peak_clock_mhz"] = pc
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic",
-            "config": {"workload": workload, "global_batch": 2 * world, "seq_len": 4096,
+            "config": {"workload": HEADLINE, "global_batch": 2 * world, "seq_len": 4096,
                        "parallelism": f"replicas x{world}", "l2": "256 MB buffer written before every step",
                        "flop_convention": "2*(d+dv) per unmasked (row,key) pair",
                        "algorithmic_flops": flops, "splits": res["splits"]},
-            "roofline": {"bound": "tensor", "achieved": tflops_rank, "peak": fp8_peak, "unit": "TFLOP/s",
-                         "frac": tflops_rank / fp8_peak, "traffic": _profiled_traffic("prefill"),
-                         "kernel": PROFILED_TRAFFIC["prefill"]["kernel"],
-                         "peak_source": f"{peaks['source']} bf16 burst x2 (dense FP8 = 2x bf16)"},
+            "roofline": roof,
             "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e_ms,
                     "mode": f"pipelined: {E2E_SETS} buffer sets, copy-in / compute / copy-out streams",
                     "ms_per_step_serial": e2e["ms_serial"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
-            "clocks": clk, "decode": decode, "cpu_baseline": cpu, "wall_s_timed_region": wall,
+            "clocks": clk, "decode": decode, "configs": configs, "cpu_baseline": cpu,
+            "wall_s_timed_region": wall,
         }
         print(json.dumps(line))
     if world > 1:
