@@ -197,8 +197,8 @@ def bench_case(case, steps, warmup, flush, fa8, num_splits=0, graph=False):
         name = _decode_kernel_name(case)
         per_sm = 2 if name.startswith("decode_kernel<128,128>") else 1
         g = case.Hq // case.Hkv
-        # positions per CTA: a 16-row decode tile, two 128-row tiles (prefill), or one
-        pos = 16 // g if name.startswith("decode_kernel") else (2 if name.startswith("prefill") else 1) * (128 // g)
+        # positions per work unit: a 16-row decode tile or a 128-row tile
+        pos = 16 // g if name.startswith("decode_kernel") else 128 // g
         mblocks = sum((lq + pos - 1) // pos for lq in case.seqlens_q)
         base = mblocks * case.Hkv
         launches = 2 + (1 if base * splits > per_sm * sms else 0)
@@ -366,7 +366,7 @@ def cpu_baseline_for(case, bound, budget_s, threads):
 def _decode_kernel_name(case):
     """The kernel include/fa8.h documents for this shape: the few-rows decode kernel when
     query positions x (Hq / Hkv) <= 16 with Hq / Hkv dividing 16 (batched q, dv % 128 = 0);
-    otherwise the two-tile prefill kernel for dv <= 128 and the one-tile kernel above."""
+    otherwise the persistent prefill kernel for dv <= 128 and the one-tile kernel above."""
     g = case.Hq // case.Hkv
     sq = case.seqlens_q[0]
     few = case.q_layout == "batched" and case.DV % 128 == 0 and 16 % g == 0 and sq * g <= 16

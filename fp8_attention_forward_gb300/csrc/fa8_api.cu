@@ -213,8 +213,9 @@ struct Plan {
     long long max_lk = 0;
     size_t ws_bytes = 0;
     int decode = 0;  // launch decode_kernel (at most 16 rows per kv-head, dv % 128 == 0)
-    int prefill = 0;  // launch prefill_kernel (two 128-row Q tiles per CTA, dv <= 128)
+    int prefill = 0;  // launch prefill_kernel (persistent, one 128-row Q tile per work unit, dv <= 128)
     long long base_units = 0;  // (tile of query rows, kv-head) pairs, before splitting
+    long long units = 0;       // (slot, kv-head, split) work units
 };
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -285,9 +286,8 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
         p.P = 16 / p.G;
         p.rows_per_tile = 16;
     } else if (p.DV <= 128) {
-        // two Q tiles of P positions x G heads per CTA: a slot spans 2 P positions
+        // the persistent prefill kernel: one work unit per 128-row Q tile (P positions x G heads)
         p.prefill = 1;
-        p.P = 2 * (128 / p.G);
     }
 
     // ---- Q layout
@@ -356,9 +356,8 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
     int splits;
     if (num_splits == 0) {
         // enough CTAs to fill the SMs several times over, never fewer than two tiles a split
-        // (the decode kernel, cheaper per CTA, may split up to 128 ways; a prefill CTA holds
-        // two Q tiles, so four per SM already give the same load balance)
-        const long long target = (p.prefill ? 4LL : 8LL) * sm_count;
+        // (the decode kernel, cheaper per CTA, may split up to 128 ways)
+        const long long target = 8LL * sm_count;
         const long long cap = p.decode ? 128 : 64;
         if (base_ctas >= target || max_tiles < 4) {
             splits = 1;
@@ -373,6 +372,8 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
     }
     if ((long long)splits * p.Hkv > 65535) return fail(FA8_ERR_UNSUPPORTED, "kv_heads x splits exceeds the grid limit");
     p.splits = splits;
+    p.units = p.num_slots * p.Hkv * splits;
+    if (p.prefill && p.units > 0x7fffffffLL) return fail(FA8_ERR_UNSUPPORTED, "problem too large for the unit list");
     if (splits > 1 && p.total_q > 0) {
         // fp32 O and LSE partials, then 256 bytes where the forward kernel records the split
         // cap it chose for the combine kernel
@@ -631,8 +632,8 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
             strides[1] = q->stride[1];
             strides[2] = q->stride[0];
         }
-        // one Q tile per TMA load (a prefill slot loads two)
-        const uint32_t box[4] = {(uint32_t)cw, (uint32_t)pl.G, (uint32_t)(pl.prefill ? pl.P / 2 : pl.P), 1};
+        // one Q tile per TMA load
+        const uint32_t box[4] = {(uint32_t)cw, (uint32_t)pl.G, (uint32_t)pl.P, 1};
         if ((st = encode4(&tq, q->data, dims, strides, box, cw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))) return st;
     }
     const bool kv_empty = (pl.kv_mode == 0 && pl.Sk == 0) || (pl.kv_mode == 1 && pl.total_k == 0) ||
@@ -696,6 +697,7 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
     p.window_left = window_left;
     p.num_splits = pl.splits;
     p.split_mode = pl.splits > 1;
+    p.units = (int)std::min<long long>(pl.units, 0x7fffffffLL);
     p.o = out->data;
     p.o_sb = o_sb;
     p.o_ss = o_ss;
@@ -741,11 +743,13 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
             default: return fail(FA8_ERR_UNSUPPORTED, "no decode kernel for (%d, %d)", pl.D, pl.DV);
         }
     } else if (pl.prefill) {
+        // persistent: one CTA per SM (or per unit when there are fewer), each walking the unit list
+        const dim3 pgrid((unsigned)std::max(1LL, std::min<long long>(pl.units, (long long)ds->sm_count)), 1, 1);
         switch (pl.D * 1000 + pl.DV) {
-            case 64064: e = fa8::launch_prefill<64, 64>(p, tq, tk, tv, grid, s); break;
-            case 96096: e = fa8::launch_prefill<96, 96>(p, tq, tk, tv, grid, s); break;
-            case 128128: e = fa8::launch_prefill<128, 128>(p, tq, tk, tv, grid, s); break;
-            case 192128: e = fa8::launch_prefill<192, 128>(p, tq, tk, tv, grid, s); break;
+            case 64064: e = fa8::launch_prefill<64, 64>(p, tq, tk, tv, pgrid, s); break;
+            case 96096: e = fa8::launch_prefill<96, 96>(p, tq, tk, tv, pgrid, s); break;
+            case 128128: e = fa8::launch_prefill<128, 128>(p, tq, tk, tv, pgrid, s); break;
+            case 192128: e = fa8::launch_prefill<192, 128>(p, tq, tk, tv, pgrid, s); break;
             default: return fail(FA8_ERR_UNSUPPORTED, "no prefill kernel for (%d, %d)", pl.D, pl.DV);
         }
     } else switch (pl.D * 1000 + pl.DV) {  // the one-tile kernel: dv > 128

@@ -131,6 +131,7 @@ struct FwdParams {
     int slots;
     int *split_cap;
     int cap_const;
+    int units;  // work units of the persistent prefill kernel (slot, kv-head, split)
 };
 
 struct CombineParams {

@@ -1,38 +1,38 @@
 // fa8_prefill.cuh -- the forward for many query rows per kv-head (prefill, chunked prefill)
-// with dv <= 128: two 128-row Q tiles per CTA that take turns on the tensor core.
+// with dv <= 128: a persistent kernel, one CTA per SM, each CTA walking a list of work units
+// (a 128-row Q tile of one kv-head group, one split of its keys) and streaming the units' KV
+// tiles through one pipeline, so that a unit's last tiles overlap the next unit's first ones.
 //
 // Same arithmetic as fwd_kernel ("[Cute,Fwd,Sm90] Native FP8 (E4M3 Q/K/V) forward for
 // Hopper", Design; "tml-fa4 PR #4", Summary and "Correctness fix over #1"): S = Q K^T in
 // TMEM (tcgen05.mma kind::f8f6f4), lazy running max (tau = 0.75 in log2 units), P =
-// e4m3(2^(s c - m + 8)) written over S in TMEM, O_t = P V accumulated from zero for every
-// KV tile and folded into an fp32 O as O = O * alpha + O_t (two-level accumulation), and
-// O * dv / rowsum, LSE = ln2 * (log2 rowsum + m - 8) at the end; a tile's P takes a second
-// E4M3 term (P_lo = e4m3(p - P_hi)) when the tile needs a mask or one key of some row holds
-// about an eighth or more of that row's mass so far.
+// e4m3(2^(s c - m + 8)) with the 2^8 bias folded into the packed FMA that applies the scale,
+// written over S in TMEM; O_t = P V accumulated from zero for every KV tile and folded into an
+// fp32 O as O = O * alpha + O_t (two-level accumulation); O * dv / rowsum and LSE = ln2 *
+// (log2 rowsum + m - 8) at the end.  A tile's P takes a second E4M3 term (P_lo = e4m3(p -
+// P_hi)) when the tile needs a mask or one key of some row holds about an eighth or more of
+// that row's mass so far.
 //
-// The CTA's rows are 2 x 128 (query position, q-head) pairs of one kv-head group, packed
-// position-major (PackGQA): tile A takes the first half of the CTA's positions, tile B the
-// second.  Both share every K/V tile.  Roles (384 threads, three warpgroups):
-//   warps 0-3   tile A: thread r owns TMEM lane r = row r of A; it runs the row's softmax
-//               (two passes over the S columns: the row maximum, then P), keeps the row's
-//               running O in 128 registers and folds every O_t into it, and writes the row
-//   warps 4-7   the same for tile B
-//   warp 8      TMA producer (Q of both tiles once, K/V tiles into an S-stage ring)
-//   warp 9      MMA issuer (one elected lane) and TMEM owner
-//   warps 10-11 idle (their registers go to the two tile warpgroups)
-// TMEM (512 columns): S/P of A at 0, S/P of B at 128, O_t of A at 256, O_t of B at 384.
-// A build with -DFA8_TRACE records clock64() per KV tile of the first 8 CTAs (debug only):
-// tile A, warp 0: 0 S ready, 1 max pass done, 9 / 10 P pass start / end, 2 P written, 11 the
-// tile's path (bit 0 two terms, bit 1 masked; a value, not a clock); 5-7 P written by warps
-// 1-3; issuer: 8 iteration start, 12 / 13 tile A / B's PV and next QK issued, 14 both done;
-// 15 tile B's S ready.
-// The issuer runs, per KV tile j, PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1): while one tile's
-// warpgroup turns S into P (and folds the previous O_t), the other tile's MMAs run, so every
-// sub-partition has two warps on independent work (one per tile).  FlashAttention-4 pairs
-// two Q tiles the same way ("PyTorch ... FlashAttention-4 MXFP8", 2.1 Attention Forward,
-// TMEM allocation); here each tile's O_t has its own TMEM columns and the running O lives in
-// the registers of the warpgroup that owns the tile, which is what two-level accumulation
-// needs and what lets S, O_t of both tiles fill TMEM exactly.
+// The unit list and the order of the work ("PyTorch ... FlashAttention-4 MXFP8", 2.1.2
+// Improved unroll-KV): every CTA takes units k * grid + c (even k) or k * grid + grid - 1 - c
+// (odd k) of a list ordered by decreasing key count, so the CTAs' loads even out; within a
+// CTA, the tile stream i = 0, 1, ... runs across unit boundaries: QK(i + 2) follows PV(i), so
+// the next unit's first QKs run under this unit's last softmax.
+//
+// Roles (384 threads, three warpgroups):
+//   warps 0-3   softmax: thread r owns TMEM lane r = row r of the tile; per tile it loads the
+//               row's 128 scores into registers once, takes the maximum, writes P over S
+//   warps 4-7   correction: holds the row's running O (dv fp32 registers), folds each tile's
+//               O_t into it, and writes the unit's output row
+//   warp 8      TMA producer (Q of each unit into a double buffer, K/V tiles into a ring)
+//   warp 9      PV issuer (one elected lane) and TMEM owner
+//   warp 10     QK issuer (one elected lane)
+//   warp 11     idle (its registers go to the other warpgroups)
+// TMEM (512 columns): S/P of tiles i even / odd at 0 / 128, O_t of tiles i even / odd at 256 /
+// 384.  Hand-offs: S(i) full -> softmax; alpha(i) (4-deep ring) -> correction; P(i) -> MMA;
+// O_t(i) full -> correction; O_t(i) folded -> MMA (PV(i + 2)); per unit, the row's output
+// scale and LSE (4-deep ring) softmax -> correction.  The ring depths follow from the chain
+// PV(i) <- fold(i - 2): the softmax can run at most four tiles ahead of the correction.
 #pragma once
 
 #include "fa8_kernel.cuh"
@@ -41,12 +41,14 @@ namespace fa8 {
 
 constexpr int kPfThreads = 384;
 
-// registers per thread: launch 168 (384 x 168 <= 64K); setmaxnreg gives the two tile
-// warpgroups 216 each (O in 128 of them) and 72 to the control warpgroup
+// registers per thread: launch 168 (384 x 168 <= 64K); setmaxnreg gives the softmax
+// warpgroup 184 (the row's 128 scores), the correction warpgroup 216 (the row's O in 128 of
+// them) and the control warpgroup 104
 constexpr int kPfLaunchRegs = 168;
-constexpr int kPfRegsTile = 216;
-constexpr int kPfRegsCtl = 72;
-static_assert(2 * kPfRegsTile + kPfRegsCtl == 3 * kPfLaunchRegs, "register split");
+constexpr int kPfRegsSoft = 184;
+constexpr int kPfRegsCorr = 216;
+constexpr int kPfRegsCtl = 104;
+static_assert(kPfRegsSoft + kPfRegsCorr + kPfRegsCtl == 3 * kPfLaunchRegs, "register split");
 
 template <int D, int DV>
 struct PfCfg {
@@ -58,140 +60,243 @@ struct PfCfg {
     static constexpr int CHUNK_Q = kTileM * CW;
     static constexpr int CHUNK_K = kTileN * CW;
     static constexpr int CHUNK_V = kTileN * CWV;
-    static constexpr int Q_BYTES = kTileM * D;  // one Q tile
+    static constexpr int Q_BYTES = kTileM * D;  // one Q tile (two buffers)
     static constexpr int K_BYTES = kTileN * D;
     static constexpr int V_BYTES = kTileN * DV;
-    static constexpr int MISC_BYTES = 1024;
+    static constexpr int MISC_BYTES = 8192;
     static constexpr int SMEM_LIMIT = 232448;  // max dynamic smem per block on sm_103
     static constexpr int STAGES_FIT =
         (SMEM_LIMIT - 1024 - MISC_BYTES - kTraceSmemBytes - 2 * Q_BYTES) / (K_BYTES + V_BYTES);
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
-    static constexpr int OFF_Q = 0;  // tile A, then tile B
+    static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = 2 * Q_BYTES;
     static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
     static constexpr int OFF_MISC = OFF_V + STAGES * V_BYTES;
     static constexpr int OFF_TRACE = OFF_MISC + MISC_BYTES;
     static constexpr int SMEM_BYTES = OFF_TRACE + kTraceSmemBytes + 1024;
-    static constexpr uint32_t TM_S = 0;     // S/P of tile x at TM_S + 128 x
-    static constexpr uint32_t TM_OT = 256;  // O_t of tile x at TM_OT + 128 x
+    static constexpr uint32_t TM_S = 0;     // S/P of tile i at TM_S + 128 (i % 2)
+    static constexpr uint32_t TM_OT = 256;  // O_t of tile i at TM_OT + 128 (i % 2)
     static constexpr uint32_t TM_COLS = 512;
-    // barriers: Q (2), K/V ring, then per tile S written, P written, O_t written, O_t folded
-    static constexpr int B_Q = 0;
-    static constexpr int B_KF = 2;
+    // barriers
+    static constexpr int B_QF = 0;              // Q buffer full (2)
+    static constexpr int B_QE = 2;              // Q buffer free (2)
+    static constexpr int B_KF = 4;              // K/V ring
     static constexpr int B_KE = B_KF + STAGES;
     static constexpr int B_VF = B_KE + STAGES;
     static constexpr int B_VE = B_VF + STAGES;
-    static constexpr int B_SF = B_VE + STAGES;
-    static constexpr int B_PF = B_SF + 2;
-    static constexpr int B_OF = B_PF + 2;
-    static constexpr int B_OE = B_OF + 2;
-    static constexpr int B_DONE = B_OE + 2;
-    static constexpr int NUM_BARS = B_DONE + 1;
-    static constexpr int OFF_TMEM_SLOT = 512;  // within the misc area
-    static constexpr int OFF_ABORT = 516;
-    static constexpr int OFF_VOTES = 528;  // [tile][warp] two-term votes
+    static constexpr int B_SF = B_VE + STAGES;  // S(i) written (2)
+    static constexpr int B_PF = B_SF + 2;       // P(i) written (2)
+    static constexpr int B_OF = B_PF + 2;       // O_t(i) written (2)
+    static constexpr int B_OE = B_OF + 2;       // O_t(i) folded (2)
+    static constexpr int B_AL = B_OE + 2;       // alpha(i) written (4)
+    static constexpr int B_FN = B_AL + 4;       // a unit's output scale and LSE written (4)
+    static constexpr int B_DONE = B_FN + 4;     // all MMAs of one issuer complete (2)
+    static constexpr int NUM_BARS = B_DONE + 2;
+    static constexpr int OFF_ALPHA = 512;               // [4][128] fp32
+    static constexpr int OFF_FIN = OFF_ALPHA + 2048;    // [4][2][128] fp32 (scale, LSE)
+    static constexpr int OFF_VOTES = OFF_FIN + 4096;    // [2][4] int (16-byte aligned rows)
+    static constexpr int OFF_TMEM_SLOT = OFF_VOTES + 32;
+    static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
     static_assert(STAGES >= 2, "smem too small for two K/V stages");
     static_assert(NUM_BARS * 8 <= 512, "barrier area");
+    static_assert(OFF_ABORT + 4 <= MISC_BYTES, "misc area");
     static_assert(Q_BYTES % 1024 == 0 && K_BYTES % 1024 == 0 && V_BYTES % 1024 == 0, "swizzle alignment");
 };
 
-// Key range [kv_beg, kv_end) visible to query positions [pos_first, pos_last] and its KV
-// tiles [tb, te) clipped to the split's tiles [t0, t1); empty when tb >= te.
-struct TileSpan {
-    int tb, te;
+// One work unit: a 128-row Q tile (pos_per_tile positions x G q-heads of kv-head kvh) of
+// request b, and one split of its keys.  state 0: nothing to do (no such tile, no rows, or a
+// split the tile does not run); 1: the tile's rows see no key in this split (their output is
+// written directly); 2: KV tiles [t_beg, t_end) to run.  Whole warp must call it (varlen).
+struct PfUnit {
+    int state, b, kvh, split, q_start, Lq, Lk, k_start, pos0, pos_last, delta, t_beg, t_end;
 };
-__device__ __forceinline__ TileSpan tile_span(int pos_first, int pos_last, int Lk, int delta, int causal,
-                                              int window_left, int t0, int t1) {
-    TileSpan s{0, 0};
-    if (pos_last < pos_first) return s;
-    const int kv_end = causal ? min(Lk, pos_last + delta + 1) : Lk;
-    const int kv_beg = window_left >= 0 ? max(0, pos_first + delta - window_left) : 0;
-    if (kv_end <= kv_beg) return s;
-    s.tb = max(t0, kv_beg / kTileN);
-    s.te = min(t1, (kv_end + kTileN - 1) / kTileN);
-    if (s.te < s.tb) s.te = s.tb;
-    return s;
+__device__ __forceinline__ PfUnit pf_unit(const FwdParams &p, int u, int cap) {
+    PfUnit r;
+    r.state = 0;
+    const int per_x = p.Hkv * p.num_splits;
+    const int x = u / per_x, y = u - x * per_x;
+    int b, mb;
+    if (!p.q_varlen) {
+        b = x % p.B;
+        mb = p.mblocks_per_batch - 1 - x / p.B;
+    } else if (!varlen_slot(p, x, b, mb)) {
+        return r;
+    }
+    r.b = b;
+    r.kvh = y % p.Hkv;
+    r.split = y / p.Hkv;
+    r.q_start = p.q_varlen ? p.cu_q[b] : b * p.Sq;
+    r.Lq = p.q_varlen ? p.cu_q[b + 1] - r.q_start : p.Sq;
+    r.k_start = 0;
+    if (p.kv_mode == 0) {
+        r.Lk = p.Sk;
+    } else {
+        r.k_start = p.cu_k[b];
+        r.Lk = p.cu_k[b + 1] - r.k_start;
+    }
+    // device-side sanity of caller-provided lengths: never index outside the tensors
+    bool bad = r.Lq < 0 || r.Lk < 0 || r.q_start < 0 || r.q_start + r.Lq > p.total_q;
+    if (p.kv_mode == 1) bad |= (r.k_start < 0 || r.k_start + r.Lk > p.total_k);
+    if (p.kv_mode == 2) bad |= ((long long)r.Lk > (long long)p.max_pages * p.page_size);
+    if (bad) {
+        if ((threadIdx.x & 31) == 0) atomicOr(p.status, kStatusBounds);
+        return r;
+    }
+    r.pos0 = mb * p.pos_per_tile;
+    if (r.pos0 >= r.Lq) return r;
+    r.pos_last = min(r.pos0 + p.pos_per_tile, r.Lq) - 1;
+    r.delta = r.Lk - r.Lq;
+    const SplitRange sr =
+        split_range(r.Lq, r.Lk, r.pos0, r.pos_last, p.causal, p.window_left, p.num_splits, cap, r.split);
+    if (r.split >= sr.eff) return r;  // the combine kernel skips this split of these rows
+    r.t_beg = sr.t_beg;
+    r.t_end = sr.t_beg + sr.n_tiles;
+    r.state = r.t_end > r.t_beg ? 2 : 1;
+    return r;
 }
 
-// The P pass of one tile row (128 keys, 32 at a time) for the thread that owns the row:
-// p = 2^(s c - m) on f16 pairs (one MUFU instruction for two scores; the argument is near 0
-// where p is large, so f16 keeps it to 2^-11), P = e4m3(2^8 p) with the scaling exact in f16
-// (and P_lo = e4m3(2^8 p - P_hi) when TWO) written into the S columns, and the row sum (of p,
-// without the 2^8) over f16 groups of eight, then fp32.  The same steps fold the previous KV
-// tile's O_t into the running O (O = O alpha + O_t, 16 columns at a time; zeros before the
-// first KV tile), whose FFMAs fill issue slots the MUFU-bound exponentials leave.  The P of keys
-// [32 kq, 32 kq + 32) goes to column 32 kq (8 columns), P_lo 8 columns later: both on S columns
-// this step has read.  No branch inside: on tiles that need a mask, the max pass has already
-// written -inf over the masked S columns.
-template <int DV, bool TWO>
-__device__ __forceinline__ void p_pass(uint32_t scol, uint32_t ocol, uint64_t c2, uint64_t nm2, uint64_t a2,
-                                       uint64_t (&o2)[DV / 2], uint64_t &acc) {
+// The unit list: the k-th unit a CTA takes (snake order over the list), or -1 past its end.
+__device__ __forceinline__ int pf_unit_index(const FwdParams &p, int k) {
+    const int g = (int)gridDim.x, c = (int)blockIdx.x;
+    const long long u = (long long)k * g + ((k & 1) ? g - 1 - c : c);
+    return u < p.units ? (int)u : -1;
+}
+
+// The row maximum over the 128 scores held in registers; on tiles that need a mask, columns
+// outside [lo, hi] become -inf first (in registers: the P pass reads the same registers).
+__device__ __forceinline__ float row_max(uint32_t (&u)[128], bool need_mask, int lo, int hi) {
+    if (need_mask) {
 #pragma unroll
-    for (int kq = 0; kq < 4; ++kq) {
-        uint32_t u[32];
-        ptx::tmem_ld32(scol + 32 * kq, u);
+        for (int i = 0; i < 128; ++i)
+            if (i > hi || i < lo) u[i] = __float_as_uint(-INFINITY);
+    }
+    float m0 = ptx::fmax3(u2f(u[0]), u2f(u[1]), u2f(u[2]));
+    float m1 = ptx::fmax3(u2f(u[3]), u2f(u[4]), u2f(u[5]));
+    float m2 = ptx::fmax3(u2f(u[6]), u2f(u[7]), u2f(u[8]));
+    float m3 = ptx::fmax3(u2f(u[9]), u2f(u[10]), u2f(u[11]));
+#pragma unroll
+    for (int i = 12; i < 124; i += 8) {
+        m0 = ptx::fmax3(m0, u2f(u[i]), u2f(u[i + 1]));
+        m1 = ptx::fmax3(m1, u2f(u[i + 2]), u2f(u[i + 3]));
+        m2 = ptx::fmax3(m2, u2f(u[i + 4]), u2f(u[i + 5]));
+        m3 = ptx::fmax3(m3, u2f(u[i + 6]), u2f(u[i + 7]));
+    }
+    m0 = ptx::fmax3(m0, u2f(u[124]), u2f(u[125]));
+    m1 = ptx::fmax3(m1, u2f(u[126]), u2f(u[127]));
+    return ptx::fmax3(m0, m1, fmaxf(m2, m3));
+}
+
+// All 128 score columns of the thread's lane into registers (one wait).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&u)[128]) {
+    uint32_t(&u0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&u[0]);
+    uint32_t(&u1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&u[32]);
+    uint32_t(&u2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&u[64]);
+    uint32_t(&u3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&u[96]);
+    ptx::tmem_ld32(taddr, u0);
+    ptx::tmem_ld32(taddr + 32, u1);
+    ptx::tmem_ld32(taddr + 64, u2);
+    ptx::tmem_ld32(taddr + 96, u3);
+    ptx::tmem_wait_ld();
+    ptx::reg_fence32(u0);
+    ptx::reg_fence32(u1);
+    ptx::reg_fence32(u2);
+    ptx::reg_fence32(u3);
+}
+
+// O = O alpha + O_t for the whole row, 64 columns per TMEM round trip, then one packed FMA per
+// column pair.
+template <int DV>
+__device__ __forceinline__ void fold_pass(uint32_t ocol, uint64_t a2, uint64_t (&o2)[DV / 2]) {
+#pragma unroll
+    for (int h = 0; h < DV / 64; ++h) {
+        uint32_t t0[32], t1[32];
+        ptx::tmem_ld32(ocol + 64 * h, t0);
+        ptx::tmem_ld32(ocol + 64 * h + 32, t1);
         ptx::tmem_wait_ld();
-        ptx::reg_fence32(u);
-        uint32_t w[8], wl[8];
-        uint32_t e4_prev = 0u;
+        ptx::reg_fence32(t0);
+        ptx::reg_fence32(t1);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float y0, y1, y2, y3;
-            ptx::f2unpack(ptx::ffma2(ptx::f2pack(__uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1])), c2, nm2),
-                          y0, y1);
-            ptx::f2unpack(ptx::ffma2(ptx::f2pack(__uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3])), c2, nm2),
-                          y2, y3);
-            const uint32_t e01 = ptx::ex2_h2(ptx::cvt_f16x2(y1, y0));
-            const uint32_t e23 = ptx::ex2_h2(ptx::cvt_f16x2(y3, y2));
-            const uint32_t e4 = ptx::hadd2(e01, e23);
-            if (k & 1) {
-                float s0, s1;
-                ptx::h2_to_f32(ptx::hadd2(e4_prev, e4), s0, s1);
-                acc = ptx::fadd2(acc, ptx::f2pack(s0, s1));
-            } else {
-                e4_prev = e4;
-            }
-            const uint32_t q01 = ptx::hmul2(e01, 0x5C005C00u), q23 = ptx::hmul2(e23, 0x5C005C00u);  // x 2^8, exact
-            w[k] = ptx::prmt_lo16(ptx::cvt_e4m3x2_h2(q01), ptx::cvt_e4m3x2_h2(q23));
-            if (TWO) {
-                const uint32_t d01 = ptx::hsub2(q01, ptx::e4m3x2_to_h2(w[k] & 0xFFFFu));
-                const uint32_t d23 = ptx::hsub2(q23, ptx::e4m3x2_to_h2(w[k] >> 16));
-                wl[k] = ptx::prmt_lo16(ptx::cvt_e4m3x2_h2(d01), ptx::cvt_e4m3x2_h2(d23));
-            } else {
-                wl[k] = 0u;  // another warp of this tile may vote for two terms: this warp's is zero
-            }
+        for (int i = 0; i < 16; ++i) {
+            o2[32 * h + i] = ptx::ffma2(o2[32 * h + i], a2, ptx::f2pack(u2f(t0[2 * i]), u2f(t0[2 * i + 1])));
+            o2[32 * h + 16 + i] = ptx::ffma2(o2[32 * h + 16 + i], a2, ptx::f2pack(u2f(t1[2 * i]), u2f(t1[2 * i + 1])));
         }
-        ptx::tmem_st8(scol + 32 * kq, w);
-        ptx::tmem_st8(scol + 32 * kq + 8, wl);
+    }
+    if (DV % 64) {  // a last 32 columns (dv = 96)
+        uint32_t t0[32];
+        ptx::tmem_ld32(ocol + DV - 32, t0);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence32(t0);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int c0 = 32 * kq + 16 * hh;
-            if (c0 < DV) {
-                uint32_t v[16];
-                ptx::tmem_ld16(ocol + c0, v);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence16(v);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    o2[c0 / 2 + i] =
-                        ptx::ffma2(o2[c0 / 2 + i], a2, ptx::f2pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])));
-            }
-        }
+        for (int i = 0; i < 16; ++i)
+            o2[(DV - 32) / 2 + i] = ptx::ffma2(o2[(DV - 32) / 2 + i], a2, ptx::f2pack(u2f(t0[2 * i]), u2f(t0[2 * i + 1])));
     }
 }
 
-// O = O alpha + O_t for the whole row (the last KV tile's fold).
-template <int DV>
-__device__ __forceinline__ void fold_all(uint32_t ocol, uint64_t a2, uint64_t (&o2)[DV / 2]) {
+// P for one 32-key chunk of the row: p = 2^(s c - m + 8) in fp32, the 2^8 bias folded into the
+// same packed FMA that applies the scale and subtracts the running maximum; w = e4m3(p) (round
+// to nearest even, saturating) and, when `two`, wl = e4m3(p - P_hi) (zeros otherwise: another
+// warp of the tile may have voted for two terms); the unrounded p go into two packed fp32
+// row-sum accumulators.  Masked keys hold -inf, so their p is exactly 0.  The p overwrite
+// their scores in u, so the P_lo step reads them back without a second copy.
+__device__ __forceinline__ void p_chunk(uint32_t (&u)[32], uint64_t c2, uint64_t b2, bool two, uint64_t &acc0,
+                                        uint64_t &acc1, uint32_t (&w)[8], uint32_t (&wl)[8]) {
 #pragma unroll
-    for (int jc = 0; jc < DV / 32; ++jc) {
-        uint32_t u[32];
-        ptx::tmem_ld32(ocol + 32 * jc, u);
+    for (int k = 0; k < 8; ++k) {
+        const int o = 4 * k;
+        float y0, y1, y2, y3;
+        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[o]), u2f(u[o + 1])), c2, b2), y0, y1);
+        ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[o + 2]), u2f(u[o + 3])), c2, b2), y2, y3);
+        const float e0 = ptx::ex2(y0), e1 = ptx::ex2(y1), e2 = ptx::ex2(y2), e3 = ptx::ex2(y3);
+        acc0 = ptx::fadd2(acc0, ptx::f2pack(e0, e1));
+        acc1 = ptx::fadd2(acc1, ptx::f2pack(e2, e3));
+        w[k] = ptx::prmt_lo16(ptx::cvt_e4m3x2(e1, e0), ptx::cvt_e4m3x2(e3, e2));
+        u[o] = __float_as_uint(e0);
+        u[o + 1] = __float_as_uint(e1);
+        u[o + 2] = __float_as_uint(e2);
+        u[o + 3] = __float_as_uint(e3);
+    }
+    if (two) {
+        // the residual in f16 (p < 2^9 holds 11 significant bits there, P_hi is exact in f16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int o = 4 * k;
+            const uint32_t d01 = ptx::hsub2(ptx::cvt_f16x2(u2f(u[o + 1]), u2f(u[o])), ptx::e4m3x2_to_h2(w[k] & 0xFFFFu));
+            const uint32_t d23 = ptx::hsub2(ptx::cvt_f16x2(u2f(u[o + 3]), u2f(u[o + 2])), ptx::e4m3x2_to_h2(w[k] >> 16));
+            wl[k] = ptx::prmt_lo16(ptx::cvt_e4m3x2_h2(d01), ptx::cvt_e4m3x2_h2(d23));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) wl[k] = 0u;
+    }
+}
+
+// The P pass over the row's 128 keys, re-read from TMEM 32 columns at a time with the next
+// chunk's load in flight; a rolled loop of two chunks per iteration keeps the code that every
+// tile runs small.  P of keys [32 kq, 32 kq + 32) goes to column 32 kq (P_lo to 32 kq + 8),
+// written after the next chunk's scores have landed: columns this pass has already read.
+__device__ __forceinline__ void p_pass(uint32_t scol, uint64_t c2, uint64_t b2, bool two, uint64_t &acc0,
+                                       uint64_t &acc1) {
+    uint32_t ua[32], ub[32], w[8], wl[8];
+    ptx::tmem_ld32(scol, ua);
+    ptx::tmem_wait_ld();
+    ptx::reg_fence32(ua);
+#pragma unroll 1
+    for (int kq = 0; kq < 4; kq += 2) {
+        const uint32_t col = scol + 32u * (uint32_t)kq;
+        ptx::tmem_ld32(col + 32, ub);
+        p_chunk(ua, c2, b2, two, acc0, acc1, w, wl);
         ptx::tmem_wait_ld();
-        ptx::reg_fence32(u);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            o2[16 * jc + i] = ptx::ffma2(o2[16 * jc + i], a2, ptx::f2pack(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])));
+        ptx::reg_fence32(ub);
+        ptx::tmem_st8(col, w);
+        ptx::tmem_st8(col + 8, wl);
+        if (kq == 0) ptx::tmem_ld32(col + 64, ua);
+        p_chunk(ub, c2, b2, two, acc0, acc1, w, wl);
+        if (kq == 0) {
+            ptx::tmem_wait_ld();
+            ptx::reg_fence32(ua);
+        }
+        ptx::tmem_st8(col + 32, w);
+        ptx::tmem_st8(col + 40, wl);
     }
 }
 
@@ -207,86 +312,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // ------------------------------------------------------------ tile schedule
     int cap = p.cap_const > 0 ? p.cap_const : (1 << 20);
     if (p.num_splits > 1 && p.cap_const <= 0) {  // chosen by split_plan_kernel, which may still be running
         ptx::griddep_wait();
         cap = *p.split_cap;
     }
-    int b, mb;
-    if (!p.q_varlen) {
-        const int x = blockIdx.x;
-        b = x % p.B;
-        mb = p.mblocks_per_batch - 1 - x / p.B;
-    } else if (!varlen_slot(p, blockIdx.x, b, mb)) {
-        return;  // slot beyond the last request's position blocks
-    }
-    const int kvh = blockIdx.y % p.Hkv;
-    const int split = blockIdx.y / p.Hkv;
-    const int PP = p.pos_per_tile;  // positions per CTA (both tiles)
-    const int Pt = PP >> 1;         // positions per tile
-    const int q_start = p.q_varlen ? p.cu_q[b] : b * p.Sq;
-    const int Lq = p.q_varlen ? p.cu_q[b + 1] - q_start : p.Sq;
-    int Lk, k_start = 0;
-    if (p.kv_mode == 0) {
-        Lk = p.Sk;
-    } else {
-        k_start = p.cu_k[b];
-        Lk = p.cu_k[b + 1] - k_start;
-    }
-    bool bad = Lq < 0 || Lk < 0 || q_start < 0 || q_start + Lq > p.total_q;
-    if (p.kv_mode == 1) bad |= (k_start < 0 || k_start + Lk > p.total_k);
-    if (p.kv_mode == 2) bad |= ((long long)Lk > (long long)p.max_pages * p.page_size);
-    if (bad) {
-        if (tid == 0) atomicOr(p.status, kStatusBounds);
-        return;
-    }
-    const int pos0 = mb * PP;
-    if (pos0 >= Lq) return;
-    const int pos_last = min(pos0 + PP, Lq) - 1;
-    const int delta = Lk - Lq;
-    const SplitRange sr = split_range(Lq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits, cap, split);
-    if (split >= sr.eff) return;  // this CTA's rows run fewer splits; the combine skips this one
-    const int t_beg = sr.t_beg, t_end = sr.t_beg + sr.n_tiles;
-    // each tile's positions and its KV tiles within this split
-    // (selects, not arrays: a role picks its tile's values by a run-time index)
-    const int tp0_a = pos0, tp0_b = pos0 + Pt;
-    const int tpl_a = min(tp0_a + Pt, Lq) - 1, tpl_b = min(tp0_b + Pt, Lq) - 1;
-    const TileSpan span_a = tile_span(tp0_a, tpl_a, Lk, delta, p.causal, p.window_left, t_beg, t_end);
-    const TileSpan span_b = tile_span(tp0_b, tpl_b, Lk, delta, p.causal, p.window_left, t_beg, t_end);
-    auto tp0_of = [&](int x) { return x ? tp0_b : tp0_a; };
-    auto tpl_of = [&](int x) { return x ? tpl_b : tpl_a; };
-    auto span_of = [&](int x) { return x ? span_b : span_a; };
-    const bool has_sink = p.sink != nullptr && (!p.split_mode || split == 0);
-
-    // per-row facts (tile warpgroups): row r of tile x
-    const int side = (warp >> 2) & 1;
-    const int r = tid & 127;
-    const int rpos = tp0_of(side) + r / p.G;
-    const int hq = kvh * p.G + r % p.G;
-    const bool row_ok = warp < 8 && r < p.rows_per_tile && rpos < Lq;
-    const int tok = q_start + rpos;
-    const long long beta = p.q_varlen ? 0 : b;
-    const long long rho = p.q_varlen ? tok : rpos;
-
-    // writes a row whose keys in this split are all masked: O = 0, LSE = -inf (or the sink)
-    auto write_empty_row = [&]() {
-        const float lse = has_sink ? p.sink[hq] : -INFINITY;
-        if (p.split_mode) {
-            const long long row = ((long long)split * p.total_q + tok) * p.Hq + hq;
-            p.lse_part[row] = lse;
-            float4 *dst = reinterpret_cast<float4 *>(p.o_part + row * DV);
-            for (int i = 0; i < DV / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-            if (p.lse) p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
-            uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + 2 * (beta * p.o_sb + rho * p.o_ss + hq * p.o_sh);
-            for (int i = 0; i < DV / 8; ++i) *reinterpret_cast<uint4 *>(dst + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-        }
-    };
-    if (t_end <= t_beg) {
-        if (row_ok) write_empty_row();
-        return;
-    }
+    const int PP = p.pos_per_tile;
 
     // ------------------------------------------------------------ shared memory
     uint8_t *misc = smem + C::OFF_MISC;
@@ -295,6 +326,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc + C::OFF_TMEM_SLOT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + C::OFF_ABORT);
     volatile int *votes = reinterpret_cast<volatile int *>(misc + C::OFF_VOTES);
+    const uint32_t votes_saddr = ptx::smem_u32(misc + C::OFF_VOTES);
+    float *alpha_ring = reinterpret_cast<float *>(misc + C::OFF_ALPHA);
+    float *fin_ring = reinterpret_cast<float *>(misc + C::OFF_FIN);
     const uint32_t sQ = ptx::smem_u32(smem + C::OFF_Q);
     const uint32_t sK = ptx::smem_u32(smem + C::OFF_K);
     const uint32_t sV = ptx::smem_u32(smem + C::OFF_V);
@@ -305,11 +339,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #endif
     if (tid == 0) {
         for (int x = 0; x < 2; ++x) {
-            ptx::mbar_init(BAR(C::B_Q + x), 1);
+            ptx::mbar_init(BAR(C::B_QF + x), 1);
+            ptx::mbar_init(BAR(C::B_QE + x), 1);
             ptx::mbar_init(BAR(C::B_SF + x), 1);
-            ptx::mbar_init(BAR(C::B_PF + x), 128);
+            ptx::mbar_init(BAR(C::B_PF + x), 4);  // one arrival per softmax warp
             ptx::mbar_init(BAR(C::B_OF + x), 1);
-            ptx::mbar_init(BAR(C::B_OE + x), 128);
+            ptx::mbar_init(BAR(C::B_OE + x), 4);  // one arrival per correction warp
+        }
+        for (int x = 0; x < 4; ++x) {
+            ptx::mbar_init(BAR(C::B_AL + x), 4);
+            ptx::mbar_init(BAR(C::B_FN + x), 4);
         }
         for (int i = 0; i < C::STAGES; ++i) {
             ptx::mbar_init(BAR(C::B_KF + i), 1);
@@ -318,6 +357,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ptx::mbar_init(BAR(C::B_VE + i), 1);
         }
         ptx::mbar_init(BAR(C::B_DONE), 1);
+        ptx::mbar_init(BAR(C::B_DONE + 1), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -336,270 +376,247 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Waiter W{abort_flag, p.timeout_ns, p.status};
+    // bounded waits of the row warpgroups (no pointer kept live: the abort flag by address)
+    const uint32_t abort_saddr = ptx::smem_u32(misc + C::OFF_ABORT);
+    auto wait_row = [&](uint32_t bar, uint32_t parity) -> bool {
+        bool okw = ptx::mbar_try_wait(bar, parity);
+        if (!okw) okw = wait_slow_s(bar, parity, abort_saddr, p.timeout_ns, p.status);
+        return __all_sync(0xffffffffu, okw);
+    };
 
     if (warp >= 8) {
       ptx::setmaxnreg_dec<kPfRegsCtl>();
       if (warp == 8) {
         // ======================================================== TMA producer
         const bool paged = p.kv_mode == 2;
-        int issued_k = 0, issued_v = 0;
-        if (lane == 0) {
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                if (span_of(x).te <= span_of(x).tb) continue;  // this tile has no keys in this split
-                ptx::mbar_arrive_expect_tx(BAR(C::B_Q + x), (uint32_t)(D * p.rows_per_tile));
-                const int c2 = p.q_varlen ? q_start + tp0_of(x) : tp0_of(x);
-                const int c3 = p.q_varlen ? 0 : b;
+        int issued_k = 0, issued_v = 0, issued_q = 0;
+        bool ok = true;
+        int it = 0, uidx = 0;
+        for (int k = 0; ok; ++k) {
+            const int u = pf_unit_index(p, k);
+            if (u < 0) break;
+            const PfUnit un = pf_unit(p, u, cap);
+            if (un.state != 2) continue;
+            // this unit's Q into buffer uidx % 2, once the unit two back has issued its last QK
+            const int qb = uidx & 1;
+            if (!W.wait_warp(BAR(C::B_QE + qb), (((uint32_t)uidx >> 1) & 1u) ^ 1u)) { ok = false; break; }
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(BAR(C::B_QF + qb), (uint32_t)(D * p.rows_per_tile));
+                const int c2 = p.q_varlen ? un.q_start + un.pos0 : un.pos0;
+                const int c3 = p.q_varlen ? 0 : un.b;
 #pragma unroll
                 for (int c = 0; c < C::NCK; ++c)
-                    ptx::tma_load_4d(sQ + x * C::Q_BYTES + c * C::CHUNK_Q, &tm_q, BAR(C::B_Q + x), c * C::CW,
-                                     kvh * p.G, c2, c3);
+                    ptx::tma_load_4d(sQ + qb * C::Q_BYTES + c * C::CHUNK_Q, &tm_q, BAR(C::B_QF + qb), c * C::CW,
+                                     un.kvh * p.G, c2, c3);
             }
-        }
-        for (int j = t_beg; j < t_end; ++j) {
-            const int it = j - t_beg;
-            const int k0 = j * kTileN;
-            const int st = it % C::STAGES;
-            const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-            int page = 0, prow = 0;
-            if (paged && lane < p.boxes_per_tile) {
-                const int j0 = k0 + lane * p.box_n;
-                const int pi = j0 / p.page_size;
-                prow = j0 - pi * p.page_size;
-                page = p.num_pages;  // past the request's keys: out of range, TMA fills zeros
-                if (j0 < Lk) {
-                    const int e = p.block_table[(long long)b * p.bt_stride + pi];
-                    if (e >= 0 && e < p.num_pages) page = e;
-                    else atomicOr(p.status, kStatusBounds);
-                }
-            }
-            const int c2 = p.kv_mode == 1 ? k_start + k0 : k0;
-            const int c3 = p.kv_mode == 1 ? 0 : b;
-            if (!W.wait_warp(BAR(C::B_KE + st), ph ^ 1u)) break;
-            if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_KF + st), (uint32_t)C::K_BYTES);
             __syncwarp();
-            const uint32_t dK = sK + st * C::K_BYTES;
-            if (paged) {
-                if (lane < p.boxes_per_tile) {
+            issued_q = ++uidx;
+            for (int j = un.t_beg; j < un.t_end; ++j, ++it) {
+                const int k0 = j * kTileN;
+                const int st = it % C::STAGES;
+                const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+                int page = 0, prow = 0;
+                if (paged && lane < p.boxes_per_tile) {
+                    const int j0 = k0 + lane * p.box_n;
+                    const int pi = j0 / p.page_size;
+                    prow = j0 - pi * p.page_size;
+                    page = p.num_pages;  // past the request's keys: out of range, TMA fills zeros
+                    if (j0 < un.Lk) {
+                        const int e = p.block_table[(long long)un.b * p.bt_stride + pi];
+                        if (e >= 0 && e < p.num_pages) page = e;
+                        else atomicOr(p.status, kStatusBounds);
+                    }
+                }
+                const int c2 = p.kv_mode == 1 ? un.k_start + k0 : k0;
+                const int c3 = p.kv_mode == 1 ? 0 : un.b;
+                if (!W.wait_warp(BAR(C::B_KE + st), ph ^ 1u)) { ok = false; break; }
+                if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_KF + st), (uint32_t)C::K_BYTES);
+                __syncwarp();
+                const uint32_t dK = sK + st * C::K_BYTES;
+                if (paged) {
+                    if (lane < p.boxes_per_tile) {
+#pragma unroll
+                        for (int c = 0; c < C::NCK; ++c)
+                            ptx::tma_load_4d(dK + c * C::CHUNK_K + lane * p.box_n * C::CW, &tm_k, BAR(C::B_KF + st),
+                                             c * C::CW, un.kvh, prow, page);
+                    }
+                } else if (lane == 0) {
 #pragma unroll
                     for (int c = 0; c < C::NCK; ++c)
-                        ptx::tma_load_4d(dK + c * C::CHUNK_K + lane * p.box_n * C::CW, &tm_k, BAR(C::B_KF + st),
-                                         c * C::CW, kvh, prow, page);
+                        ptx::tma_load_4d(dK + c * C::CHUNK_K, &tm_k, BAR(C::B_KF + st), c * C::CW, un.kvh, c2, c3);
                 }
-            } else if (lane == 0) {
+                issued_k = it + 1;
+                if (!W.wait_warp(BAR(C::B_VE + st), ph ^ 1u)) { ok = false; break; }
+                if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_VF + st), (uint32_t)C::V_BYTES);
+                __syncwarp();
+                const uint32_t dV = sV + st * C::V_BYTES;
+                if (paged) {
+                    if (lane < p.boxes_per_tile) {
 #pragma unroll
-                for (int c = 0; c < C::NCK; ++c)
-                    ptx::tma_load_4d(dK + c * C::CHUNK_K, &tm_k, BAR(C::B_KF + st), c * C::CW, kvh, c2, c3);
-            }
-            issued_k = it + 1;
-            if (!W.wait_warp(BAR(C::B_VE + st), ph ^ 1u)) break;
-            if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_VF + st), (uint32_t)C::V_BYTES);
-            __syncwarp();
-            const uint32_t dV = sV + st * C::V_BYTES;
-            if (paged) {
-                if (lane < p.boxes_per_tile) {
+                        for (int c = 0; c < C::NCV; ++c)
+                            ptx::tma_load_4d(dV + c * C::CHUNK_V + lane * p.box_n * C::CWV, &tm_v, BAR(C::B_VF + st),
+                                             c * C::CWV, un.kvh, prow, page);
+                    }
+                } else if (lane == 0) {
 #pragma unroll
                     for (int c = 0; c < C::NCV; ++c)
-                        ptx::tma_load_4d(dV + c * C::CHUNK_V + lane * p.box_n * C::CWV, &tm_v, BAR(C::B_VF + st),
-                                         c * C::CWV, kvh, prow, page);
+                        ptx::tma_load_4d(dV + c * C::CHUNK_V, &tm_v, BAR(C::B_VF + st), c * C::CWV, un.kvh, c2, c3);
                 }
-            } else if (lane == 0) {
-#pragma unroll
-                for (int c = 0; c < C::NCV; ++c)
-                    ptx::tma_load_4d(dV + c * C::CHUNK_V, &tm_v, BAR(C::B_VF + st), c * C::CWV, kvh, c2, c3);
+                issued_v = it + 1;
             }
-            issued_v = it + 1;
         }
         if (*abort_flag) {
             // every load already issued must land before the CTA's smem is released
-#pragma unroll
-            for (int x = 0; x < 2; ++x)
-                if (span_of(x).te > span_of(x).tb) W.drain(BAR(C::B_Q + x), 0);
+            for (int i = max(0, issued_q - 2); i < issued_q; ++i)
+                W.drain(BAR(C::B_QF + (i & 1)), (uint32_t)(i >> 1) & 1u);
             for (int i = max(0, issued_k - C::STAGES); i < issued_k; ++i)
                 W.drain(BAR(C::B_KF + i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u);
             for (int i = max(0, issued_v - C::STAGES); i < issued_v; ++i)
                 W.drain(BAR(C::B_VF + i % C::STAGES), (uint32_t)(i / C::STAGES) & 1u);
         }
         __syncwarp();
-      } else if (warp == 9) {
-        // ======================================================== MMA issuer (one elected lane)
-        // Per KV tile j: PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1).  The tensor core takes one
-        // issuer's MMAs in order and its queue is short (an issue waits for room), so this
-        // order keeps tile B one MMA phase behind tile A: B's softmax runs while A's PV and QK
-        // run, and the other way round.
+      } else if (warp == 9 || warp == 10) {
+        // ======================================================== MMA issuers (one elected lane each)
+        // warp 9 issues PV(i) for every tile; warp 10 issues QK(i + 2) once PV(i) has completed
+        // (QK(i + 2) overwrites the S/P columns PV(i) reads), so neither waits on the other's
+        // issue costs.
         constexpr uint32_t kIdescQK = idesc_e4m3(kTileM, kTileN, false);
         constexpr uint32_t kIdescPV = idesc_e4m3(kTileM, DV, true);
-        const uint64_t dk0 = sdesc(sK, 16, 8 * C::CW, swz_layout(C::CW));
-        const uint64_t dv0 = sdesc(sV, C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
         const bool leader = ptx::elect_one();
         bool ok = true;
+        const bool is_qk = warp == 10;
+        const uint64_t dk0 = sdesc(sK, 16, 8 * C::CW, swz_layout(C::CW));
+        const uint64_t dv0 = sdesc(sV, C::CHUNK_V, 8 * C::CWV, swz_layout(C::CWV));
+        int i = 0, uidx = 0;
+        for (int k = 0; ok; ++k) {
+            const int u = pf_unit_index(p, k);
+            if (u < 0) break;
+            const PfUnit un = pf_unit(p, u, cap);
+            if (un.state != 2) continue;
+            const int qb = uidx & 1;
+            ++uidx;
+            for (int j = un.t_beg; j < un.t_end; ++j, ++i) {
+                if (is_qk) {
+                    // S(i) = Q K_j^T; it overwrites P(i - 2): PV(i - 2) must be complete
+                    if (i >= 2 && !W.wait_warp(BAR(C::B_OF + (i & 1)), (((uint32_t)i >> 1) & 1u) ^ 1u)) { ok = false; break; }
+                    if (j == un.t_beg && !W.wait_warp(BAR(C::B_QF + qb), ((uint32_t)(uidx - 1) >> 1) & 1u)) { ok = false; break; }
+                    const int ks = i % C::STAGES;
+                    if (!W.wait_warp(BAR(C::B_KF + ks), (uint32_t)(i / C::STAGES) & 1u)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint64_t dq = sdesc(sQ + qb * C::Q_BYTES, 16, 8 * C::CW, swz_layout(C::CW));
+                    const uint64_t dk = dk0 + (uint64_t)((ks * C::K_BYTES) >> 4);
+                    if (leader) {
 #pragma unroll
-        for (int x = 0; x < 2; ++x)
-            if (ok && span_of(x).te > span_of(x).tb) ok = W.wait_warp(BAR(C::B_Q + x), 0);
-        ptx::tc_fence_after();
-        auto in_tile = [&](int x, int j) { return j >= span_of(x).tb && j < span_of(x).te; };
-        // S_x = Q_x K_j^T
-        auto qk = [&](int x, int j) {
-            const int ks = (j - t_beg) % C::STAGES;
-            const uint64_t dq = sdesc(sQ + x * C::Q_BYTES, 16, 8 * C::CW, swz_layout(C::CW));
-            const uint64_t dk = dk0 + (uint64_t)((ks * C::K_BYTES) >> 4);
-            if (leader) {
+                        for (int kk = 0; kk < D / 32; ++kk) {
+                            const uint32_t off = (uint32_t)((((kk * 32) / C::CW) * C::CHUNK_Q + (kk * 32) % C::CW) >> 4);
+                            ptx::mma_f8_ss(tmem + C::TM_S + (uint32_t)(i & 1) * 128u, dq + off, dk + off, kIdescQK,
+                                           kk > 0 ? 1u : 0u);
+                        }
+                        ptx::tc_commit(BAR(C::B_SF + (i & 1)));
+                        ptx::tc_commit(BAR(C::B_KE + ks));
+                        if (j + 1 == un.t_end) ptx::tc_commit(BAR(C::B_QE + qb));  // the unit's last QK
+                    }
+                    __syncwarp();
+                } else {
+                    // O_t(i) = P(i) V_j (+ P_lo V_j): waits for P(i) and for the fold of O_t(i - 2).
+                    // The P_hi MMAs go first; the two-term decision (the mask, or any warp's vote) is
+                    // read while they run, and the P_lo MMAs (onto the same O_t) follow if needed.
+                    const int vs = i % C::STAGES;
+                    if (!W.wait_warp(BAR(C::B_VF + vs), (uint32_t)(i / C::STAGES) & 1u)) { ok = false; break; }
+                    if (!W.wait_warp(BAR(C::B_PF + (i & 1)), ((uint32_t)i >> 1) & 1u)) { ok = false; break; }
+                    if (i >= 2 && !W.wait_warp(BAR(C::B_OE + (i & 1)), (((uint32_t)i >> 1) & 1u) ^ 1u)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint64_t dv = dv0 + (uint64_t)((vs * C::V_BYTES) >> 4);
+                    const uint32_t s_col = tmem + C::TM_S + (uint32_t)(i & 1) * 128u;
+                    const uint32_t otile = tmem + C::TM_OT + (uint32_t)(i & 1) * 128u;
+                    if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
-                    const uint32_t off = (uint32_t)((((kk * 32) / C::CW) * C::CHUNK_Q + (kk * 32) % C::CW) >> 4);
-                    ptx::mma_f8_ss(tmem + C::TM_S + x * 128, dq + off, dk + off, kIdescQK, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < kTileN / 32; ++kk)
+                            ptx::mma_f8_ts(otile, s_col + kk * 32, dv + (uint64_t)((kk * 32 * C::CWV) >> 4), kIdescPV,
+                                           kk > 0 ? 1u : 0u);
+                    }
+                    bool two_term =
+                        tile_needs_mask(j * kTileN, un.Lk, p.causal, p.window_left, un.pos0, un.pos_last, un.delta);
+                    if (!two_term) {
+                        const int4 vt = ptx::ld_shared_v4_volatile(votes_saddr + 16u * (uint32_t)(i & 1));
+                        two_term = (vt.x | vt.y | vt.z | vt.w) != 0;
+                    }
+                    if (leader) {
+                        if (two_term) {  // + P_lo V (P_lo 8 columns after each P_hi slice)
+#pragma unroll
+                            for (int kk = 0; kk < kTileN / 32; ++kk)
+                                ptx::mma_f8_ts(otile, s_col + kk * 32 + 8, dv + (uint64_t)((kk * 32 * C::CWV) >> 4),
+                                               kIdescPV, 1u);
+                        }
+                        ptx::tc_commit(BAR(C::B_OF + (i & 1)));
+                        ptx::tc_commit(BAR(C::B_VE + vs));
+                    }
+                    __syncwarp();
                 }
-                ptx::tc_commit(BAR(C::B_SF + x));
             }
-            __syncwarp();
-        };
-        // O_t,x = P_x V_j (+ P_lo V_j): waits for P and for the fold of the previous O_t
-        auto pv = [&](int x, int j) -> bool {
-            const int n = j - span_of(x).tb;
-            if (!W.wait_warp(BAR(C::B_PF + x), (uint32_t)n & 1u)) return false;
-            if (!W.wait_warp(BAR(C::B_OE + x), ((uint32_t)n & 1u) ^ 1u)) return false;
-            ptx::tc_fence_after();
-            const bool two_term =
-                tile_needs_mask(j * kTileN, Lk, p.causal, p.window_left, tp0_of(x), tpl_of(x), delta) ||
-                (votes[x * 4 + 0] | votes[x * 4 + 1] | votes[x * 4 + 2] | votes[x * 4 + 3]) != 0;
-            const int vs = (j - t_beg) % C::STAGES;
-            const uint64_t dv = dv0 + (uint64_t)((vs * C::V_BYTES) >> 4);
-            const uint32_t s_col = tmem + C::TM_S + x * 128;
-            const uint32_t otile = tmem + C::TM_OT + x * 128;
-            if (leader) {
-#pragma unroll
-                for (int kk = 0; kk < kTileN / 32; ++kk)
-                    ptx::mma_f8_ts(otile, s_col + kk * 32, dv + (uint64_t)((kk * 32 * C::CWV) >> 4), kIdescPV,
-                                   kk > 0 ? 1u : 0u);
-                if (two_term) {  // + P_lo V (P_lo 8 columns after each P_hi slice)
-#pragma unroll
-                    for (int kk = 0; kk < kTileN / 32; ++kk)
-                        ptx::mma_f8_ts(otile, s_col + kk * 32 + 8, dv + (uint64_t)((kk * 32 * C::CWV) >> 4),
-                                       kIdescPV, 1u);
-                }
-                ptx::tc_commit(BAR(C::B_OF + x));
-            }
-            __syncwarp();
-            return true;
-        };
-        // prologue: S of the first KV tile for each Q tile that starts there
-        if (ok) ok = W.wait_warp(BAR(C::B_KF + 0), 0u);
-        if (ok) {
-            ptx::tc_fence_after();
-#pragma unroll
-            for (int x = 0; x < 2; ++x)
-                if (in_tile(x, t_beg)) qk(x, t_beg);
-            if (leader) ptx::tc_commit(BAR(C::B_KE + 0));
-            __syncwarp();
         }
-        for (int j = t_beg; ok && j < t_end; ++j) {
-            const int it = j - t_beg;
-            const bool more = j + 1 < t_end;
-            if (lane == 0) FA8_EV(8, it);
-            if (!W.wait_warp(BAR(C::B_VF + it % C::STAGES), (uint32_t)(it / C::STAGES) & 1u)) { ok = false; break; }
-            if (more && !W.wait_warp(BAR(C::B_KF + (it + 1) % C::STAGES), (uint32_t)((it + 1) / C::STAGES) & 1u)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                if (in_tile(x, j) && !pv(x, j)) { ok = false; break; }
-                if (lane == 0) FA8_EV(12 + x, it);
-                if (more && in_tile(x, j + 1)) qk(x, j + 1);
-            }
-            if (!ok) break;
-            if (lane == 0) FA8_EV(14, it);
-            if (leader) {
-                ptx::tc_commit(BAR(C::B_VE + it % C::STAGES));
-                if (more) ptx::tc_commit(BAR(C::B_KE + (it + 1) % C::STAGES));
-            }
-            __syncwarp();
-        }
-        // all MMAs must finish before TMEM is released
-        if (leader) ptx::tc_commit(BAR(C::B_DONE));
+        // this issuer's MMAs must finish before TMEM is released
+        const uint32_t done = BAR(C::B_DONE + (warp - 9));
+        if (leader) ptx::tc_commit(done);
         __syncwarp();
-        W.drain(BAR(C::B_DONE), 0);
+        W.drain(done, 0);
         __syncwarp();
       }
-    } else {
-      ptx::setmaxnreg_inc<kPfRegsTile>();
-      {
-        // bounded waits that keep no pointer live in registers (the fields come from the
-        // parameters and the shared abort flag's address on the slow path)
-        const uint32_t abort_saddr = ptx::smem_u32(misc + C::OFF_ABORT);
-        auto wait_tile = [&](uint32_t bar, uint32_t parity) -> bool {
-            bool okw = ptx::mbar_try_wait(bar, parity);
-            if (!okw) okw = wait_slow_s(bar, parity, abort_saddr, p.timeout_ns, p.status);
-            return __all_sync(0xffffffffu, okw);
-        };
-        // ======================================================== tile warpgroup (softmax + fold)
-        const int x = side;
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t scol = tmem + lane_base + C::TM_S + x * 128;
-        const uint32_t ocol = tmem + lane_base + C::TM_OT + x * 128;
-        const int tb = span_of(x).tb, nt = span_of(x).te - span_of(x).tb;
-        const int xp0 = tp0_of(x), xpl = tpl_of(x);
-        const float dqv = p.dq ? p.dq[b * p.dq_sb + kvh * p.dq_sh] : 1.f;
-        const float dkv = p.dk ? p.dk[b * p.dk_sb + kvh * p.dk_sh] : 1.f;
+    } else if (warp < 4) {
+      ptx::setmaxnreg_inc<kPfRegsSoft>();
+      // ======================================================== softmax warpgroup
+      const int r = tid;  // TMEM lane = row
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      bool ok = true;
+      int i = 0, uidx = 0;
+      for (int kk = 0; ok; ++kk) {
+        const int u = pf_unit_index(p, kk);
+        if (u < 0) break;
+        const PfUnit un = pf_unit(p, u, cap);
+        if (un.state != 2) continue;
+        const int rpos = un.pos0 + r / p.G;
+        const int hq = un.kvh * p.G + r % p.G;
+        const bool row_ok = r < p.rows_per_tile && rpos < un.Lq;
+        const float dqv = p.dq ? p.dq[un.b * p.dq_sb + un.kvh * p.dq_sh] : 1.f;
+        const float dkv = p.dk ? p.dk[un.b * p.dk_sb + un.kvh * p.dk_sh] : 1.f;
         const float c = p.scale_log2 * dqv * dkv;
         const uint64_t c2 = ptx::f2pack(c, c);
-        const int hi_row = p.causal ? min(Lk - 1, rpos + delta) : Lk - 1;
-        const int lo_row = p.window_left >= 0 ? max(0, rpos + delta - p.window_left) : 0;
-        uint64_t o2[DV / 2];  // the row's running O, as packed fp32 pairs (columns 2i, 2i+1)
-#pragma unroll
-        for (int i = 0; i < DV / 2; ++i) o2[i] = ptx::f2pack(0.f, 0.f);
+        const int hi_row = p.causal ? min(un.Lk - 1, rpos + un.delta) : un.Lk - 1;
+        const int lo_row = p.window_left >= 0 ? max(0, rpos + un.delta - p.window_left) : 0;
         float m_run = -INFINITY, row_sum = 0.f;
-        float alpha_prev = 0.f;  // rescale of the KV tile whose O_t the next fold adds
-        {
-            // O_t starts at zero, so the first KV tile's P pass folds zeros
-            uint32_t z[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) z[i] = 0u;
-#pragma unroll
-            for (int jc = 0; jc < DV / 32; ++jc) ptx::tmem_st32(ocol + 32 * jc, z);
-            ptx::tmem_wait_st();
-        }
-        bool ok = true;
-        for (int n = 0; ok && n < nt; ++n) {
-            const int k0 = (tb + n) * kTileN;
-            if (!wait_tile(BAR(C::B_SF + x), (uint32_t)n & 1u)) { ok = false; break; }
-            const bool tr = tid == 0;
-            if (tr) FA8_EV(0, n);
-            if (tid == 128) FA8_EV(15, n);
+        for (int j = un.t_beg; j < un.t_end; ++j, ++i) {
+            const int k0 = j * kTileN;
+            if (!wait_row(BAR(C::B_SF + (i & 1)), ((uint32_t)i >> 1) & 1u)) { ok = false; break; }
             ptx::tc_fence_after();
+            const uint32_t scol = tmem + lane_base + C::TM_S + (uint32_t)(i & 1) * 128u;
             const bool need_mask =
-                tile_needs_mask(k0, Lk, p.causal, p.window_left, xp0, xpl, delta);
-            const int hi = hi_row - k0, lo = lo_row - k0;  // visible columns: [lo, hi]
-            // ---- pass 1: the row's maximum over the tile, 32 columns at a time; on tiles that
-            // need a mask, the masked columns are written back as -inf for the P pass
+                tile_needs_mask(k0, un.Lk, p.causal, p.window_left, un.pos0, un.pos_last, un.delta);
             float mx = -INFINITY;
+            if (!need_mask) {
+                uint32_t u[128];
+                tmem_ld128(scol, u);
+                mx = row_max(u, false, 0, 0);
+            } else {
+                // tiles with masked columns: 32 at a time, the masked ones written back as -inf
+                // for the P pass (a rolled loop: this path is rare and its code stays small)
+                const int lo = lo_row - k0, hi = hi_row - k0;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                uint32_t u[32];
-                ptx::tmem_ld32(scol + 32 * q, u);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence32(u);
-                if (need_mask) {
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(scol + 32 * q, v);
+                    ptx::tmem_wait_ld();
+                    ptx::reg_fence32(v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = 32 * q + i;
-                        if (col > hi || col < lo) u[i] = __float_as_uint(-INFINITY);
+                    for (int e = 0; e < 32; ++e) {
+                        const int col = 32 * q + e;
+                        if (col > hi || col < lo) v[e] = __float_as_uint(-INFINITY);
+                        mx = fmaxf(mx, u2f(v[e]));
                     }
-                    ptx::tmem_st32(scol + 32 * q, u);
+                    ptx::tmem_st32(scol + 32 * q, v);
                 }
-                float ma = ptx::fmax3(u2f(u[0]), u2f(u[1]), u2f(u[2]));
-                float mb2 = ptx::fmax3(u2f(u[16]), u2f(u[17]), u2f(u[18]));
-#pragma unroll
-                for (int i = 3; i < 15; i += 2) {
-                    ma = ptx::fmax3(ma, u2f(u[i]), u2f(u[i + 1]));
-                    mb2 = ptx::fmax3(mb2, u2f(u[16 + i]), u2f(u[16 + i + 1]));
-                }
-                mx = ptx::fmax3(mx, ptx::fmax3(ma, mb2, u2f(u[15])), u2f(u[31]));
+                ptx::tmem_wait_st();
             }
-            if (need_mask) ptx::tmem_wait_st();
-            if (tr) FA8_EV(1, n);
-            // ---- lazy rescale and the two-term vote
+            // lazy rescale; alpha(i) to the correction warpgroup
             const float mt = mx * c;
             float alpha = 1.f;
             if (mt > m_run + kTau) {
@@ -607,97 +624,147 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 row_sum *= alpha;
                 m_run = mt;
             }
+            alpha_ring[(i & 3) * 128 + r] = alpha;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(BAR(C::B_AL + (i & 3)));
+            // two-term vote: the tile's largest p is 2^(mt - m + 8); it holds more than about 1/8 of
+            // the row's mass so far when log2 of it exceeds log2(row_sum) - log2(7).  log2(row_sum)
+            // is taken as its fp32 exponent (the floor), without a MUFU instruction, which errs
+            // towards two terms (an effective share between 1/15 and 1/8)
             bool two_term = need_mask;
             if (!need_mask) {
-                // the tile's largest p is 2^(mt - m + 8); it holds more than about 1/8 of the row's
-                // mass so far when log2 of it exceeds log2(row_sum) - log2(7).  log2(row_sum) is
-                // taken as its fp32 exponent (the floor), without a MUFU instruction, which errs
-                // towards two terms (an effective share between 1/15 and 1/8)
                 const int e_rs = row_sum > 0.f ? (int)((__float_as_uint(row_sum) >> 23) & 0xFF) - 127 : -1000;
                 two_term = __any_sync(0xffffffffu, row_ok && (mt - m_run + kPBias) > (float)e_rs - 2.807f);
             }
-            if (lane == 0) votes[x * 4 + (warp & 3)] = two_term ? 1 : 0;
-            // ---- pass 2 (P, see p_pass), with the fold of the previous KV tile's O_t: O_t(n - 1)
-            // stays in TMEM until this pass, so the fold is off the chain P -> PV -> QK -> S
-            if (n > 0) {
-                if (!wait_tile(BAR(C::B_OF + x), (uint32_t)(n - 1) & 1u)) { ok = false; break; }
-                ptx::tc_fence_after();
-            }
-            const float nm = m_run == -INFINITY ? 0.f : -m_run;
-            const uint64_t nm2 = ptx::f2pack(nm, nm);
-            const uint64_t a2 = ptx::f2pack(alpha_prev, alpha_prev);
-            uint64_t acc = ptx::f2pack(0.f, 0.f);
-            if (tr) FA8_EV(9, n);
-            if (two_term) p_pass<DV, true>(scol, ocol, c2, nm2, a2, o2, acc);
-            else p_pass<DV, false>(scol, ocol, c2, nm2, a2, o2, acc);
-            if (tr) FA8_EV(10, n);
-            if (tr) FA8_VAL(11, n, (two_term ? 1ull : 0ull) | (need_mask ? 2ull : 0ull));
-            alpha_prev = alpha;
-            ptx::tmem_wait_st();
+            if (lane == 0) votes[(i & 1) * 4 + warp] = two_term ? 1 : 0;
+            // P = e4m3(2^(s c + (8 - m)))
+            const float b8 = m_run == -INFINITY ? kPBias : kPBias - m_run;
+            const uint64_t b2 = ptx::f2pack(b8, b8);
+            uint64_t acc0 = ptx::f2pack(0.f, 0.f), acc1 = acc0;
+            p_pass(scol, c2, b2, two_term, acc0, acc1);
             {
-                float a0, a1;
-                ptx::f2unpack(acc, a0, a1);
-                row_sum += (a0 + a1) * 256.f;  // the f16 p carry no 2^8: scale to the biased row sum
+                float a0, a1, a2, a3;
+                ptx::f2unpack(acc0, a0, a1);
+                ptx::f2unpack(acc1, a2, a3);
+                row_sum += (a0 + a1) + (a2 + a3);  // p carry the 2^8 bias: the biased row sum
             }
+            ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(BAR(C::B_PF + x));
-            if (tr) FA8_EV(2, n);
-            if (tid == 32 || tid == 64 || tid == 96) FA8_EV(4 + (tid >> 5), n);
-            if (n > 0) ptx::mbar_arrive(BAR(C::B_OE + x));  // O_t(n - 1) folded: PV(n) may overwrite it
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(BAR(C::B_PF + (i & 1)));
         }
-        // the last KV tile's O_t
-        if (ok && nt > 0) {
-            if (wait_tile(BAR(C::B_OF + x), (uint32_t)(nt - 1) & 1u)) {
-                ptx::tc_fence_after();
-                fold_all<DV>(ocol, ptx::f2pack(alpha_prev, alpha_prev), o2);
+        if (!ok) break;
+        // the unit's output scale and LSE for the correction warpgroup; the 2^8 bias cancels
+        // between O and row_sum and is removed from the LSE
+        {
+            const bool has_sink = p.sink != nullptr && (!p.split_mode || un.split == 0);
+            const float dvv = p.dv ? p.dv[un.b * p.dv_sb + un.kvh * p.dv_sh] : 1.f;
+            const float sig = (has_sink && row_ok) ? p.sink[hq] : 0.f;
+            float scale_o = 0.f, lse;
+            if (m_run == -INFINITY) {
+                lse = has_sink ? sig : -INFINITY;
             } else {
-                ok = false;
+                const float sl2 = sig * kLog2e;
+                const float m_f = (has_sink && sl2 > m_run) ? sl2 : m_run;
+                const float sc = ptx::ex2(m_run - m_f);
+                const float rs = row_sum * sc + (has_sink ? ptx::ex2(sl2 - m_f + kPBias) : 0.f);
+                scale_o = sc * dvv / rs;
+                lse = (ptx::lg2(rs) + m_f - kPBias) * kLn2;
             }
+            fin_ring[(uidx & 3) * 256 + r] = scale_o;
+            fin_ring[(uidx & 3) * 256 + 128 + r] = lse;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(BAR(C::B_FN + (uidx & 3)));
         }
-        // ---- finalize: the 2^8 bias cancels between O and row_sum and is removed from the LSE
-        if (row_ok) {
-            if (nt == 0 || !ok) {
-                if (nt == 0) write_empty_row();
-            } else {
-                const float dvv = p.dv ? p.dv[b * p.dv_sb + kvh * p.dv_sh] : 1.f;
-                const float sig = has_sink ? p.sink[hq] : 0.f;
-                float scale_o = 0.f, lse;
-                if (m_run == -INFINITY) {
-                    lse = has_sink ? sig : -INFINITY;
-                } else {
-                    const float sl2 = sig * kLog2e;
-                    const float m_f = (has_sink && sl2 > m_run) ? sl2 : m_run;
-                    const float sc = ptx::ex2(m_run - m_f);
-                    const float rs = row_sum * sc + (has_sink ? ptx::ex2(sl2 - m_f + kPBias) : 0.f);
-                    scale_o = sc * dvv / rs;
-                    lse = (ptx::lg2(rs) + m_f - kPBias) * kLn2;
-                }
+        ++uidx;
+      }
+    } else {
+      ptx::setmaxnreg_inc<kPfRegsCorr>();
+      // ======================================================== correction warpgroup
+      const int r = tid - 128;
+      const int cw = warp - 4;
+      const uint32_t lane_base = (uint32_t)(cw * 32) << 16;
+      bool ok = true;
+      int item = 0, uidx = 0;
+      for (int k = 0; ok; ++k) {
+        const int u = pf_unit_index(p, k);
+        if (u < 0) break;
+        const PfUnit un = pf_unit(p, u, cap);
+        if (un.state == 0) continue;
+        const int rpos = un.pos0 + r / p.G;
+        const int hq = un.kvh * p.G + r % p.G;
+        const bool row_ok = r < p.rows_per_tile && rpos < un.Lq;
+        const int tok = un.q_start + rpos;
+        const long long beta = p.q_varlen ? 0 : un.b;
+        const long long rho = p.q_varlen ? tok : rpos;
+        const bool has_sink = p.sink != nullptr && (!p.split_mode || un.split == 0);
+        if (un.state == 1) {
+            // no key of this split is visible to the tile's rows: O = 0, LSE = -inf (or the sink)
+            if (row_ok) {
+                const float lse = has_sink ? p.sink[hq] : -INFINITY;
                 if (p.split_mode) {
-                    const long long row = ((long long)split * p.total_q + tok) * p.Hq + hq;
+                    const long long row = ((long long)un.split * p.total_q + tok) * p.Hq + hq;
                     p.lse_part[row] = lse;
-                    float *dst = p.o_part + row * DV;
-#pragma unroll
-                    for (int i = 0; i < DV; i += 4) {
-                        float v0, v1, v2, v3;
-                        ptx::f2unpack(o2[i / 2], v0, v1);
-                        ptx::f2unpack(o2[i / 2 + 1], v2, v3);
-                        *reinterpret_cast<float4 *>(dst + i) =
-                            make_float4(v0 * scale_o, v1 * scale_o, v2 * scale_o, v3 * scale_o);
-                    }
+                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + row * DV);
+                    for (int i = 0; i < DV / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 } else {
                     if (p.lse) p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
                     uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + 2 * (beta * p.o_sb + rho * p.o_ss + hq * p.o_sh);
+                    for (int i = 0; i < DV / 8; ++i) *reinterpret_cast<uint4 *>(dst + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            continue;
+        }
+        uint64_t o2[DV / 2];  // the row's running O, as packed fp32 pairs (columns 2i, 2i+1)
 #pragma unroll
-                    for (int i = 0; i < DV; i += 8) {
-                        float t8[8];
+        for (int q = 0; q < DV / 2; ++q) o2[q] = ptx::f2pack(0.f, 0.f);
+        const int nt = un.t_end - un.t_beg;
+        float scale_o = 0.f, lse = 0.f;
+        for (int n = 0; n < nt; ++n, ++item) {
+            const int i = item;
+            if (!wait_row(BAR(C::B_AL + (i & 3)), ((uint32_t)i >> 2) & 1u)) { ok = false; break; }
+            const float a = alpha_ring[(i & 3) * 128 + r];
+            if (!wait_row(BAR(C::B_OF + (i & 1)), ((uint32_t)i >> 1) & 1u)) { ok = false; break; }
+            ptx::tc_fence_after();
+            fold_pass<DV>(tmem + lane_base + C::TM_OT + (uint32_t)(i & 1) * 128u, ptx::f2pack(a, a), o2);
+            if (n == nt - 1) {
+                // the unit's scale and LSE: waited before this last fold is released, so the
+                // softmax cannot reach this ring slot's next use before it is read
+                if (!wait_row(BAR(C::B_FN + (uidx & 3)), ((uint32_t)uidx >> 2) & 1u)) { ok = false; break; }
+                scale_o = fin_ring[(uidx & 3) * 256 + r];
+                lse = fin_ring[(uidx & 3) * 256 + 128 + r];
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(BAR(C::B_OE + (i & 1)));
+        }
+        if (!ok) break;
+        ++uidx;
+        if (row_ok) {
+            if (p.split_mode) {
+                const long long row = ((long long)un.split * p.total_q + tok) * p.Hq + hq;
+                p.lse_part[row] = lse;
+                float *dst = p.o_part + row * DV;
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            ptx::f2unpack(o2[(i + e) / 2], t8[e], t8[e + 1]);
-                            t8[e] *= scale_o;
-                            t8[e + 1] *= scale_o;
-                        }
-                        store8(dst + 2 * i, t8, p.out_fp16);
+                for (int q = 0; q < DV; q += 4) {
+                    float v0, v1, v2, v3;
+                    ptx::f2unpack(o2[q / 2], v0, v1);
+                    ptx::f2unpack(o2[q / 2 + 1], v2, v3);
+                    *reinterpret_cast<float4 *>(dst + q) = make_float4(v0 * scale_o, v1 * scale_o, v2 * scale_o, v3 * scale_o);
+                }
+            } else {
+                if (p.lse) p.lse[beta * p.lse_sb + hq * p.lse_sh + rho * p.lse_ss] = lse;
+                uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + 2 * (beta * p.o_sb + rho * p.o_ss + hq * p.o_sh);
+#pragma unroll
+                for (int q = 0; q < DV; q += 8) {
+                    float t8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        ptx::f2unpack(o2[(q + e) / 2], t8[e], t8[e + 1]);
+                        t8[e] *= scale_o;
+                        t8[e + 1] *= scale_o;
                     }
+                    store8(dst + 2 * q, t8, p.out_fp16);
                 }
             }
         }
@@ -707,7 +774,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
 #ifdef FA8_TRACE
-    if (p.trace && blockIdx.y == 0 && blockIdx.x < kTraceCtas) {
+    if (p.trace && blockIdx.x < kTraceCtas) {
         const unsigned long long *src = reinterpret_cast<const unsigned long long *>(smem + C::OFF_TRACE);
         for (int i = tid; i < kTraceEvents * kTraceTiles; i += kPfThreads)
             p.trace[(size_t)blockIdx.x * kTraceEvents * kTraceTiles + i] = src[i];

@@ -137,8 +137,9 @@ FA8_API fa8_status fa8_fwd_workspace_size(const fa8_tensor *q, const fa8_tensor 
 /*
  * fa8_fwd_plan -- the launch plan fa8_fwd would use on a device with `sm_count` SMs,
  * computed on the host only (no CUDA call): the split count, the workspace bytes and the
- * forward grid (grid_out[0] = Q-tile slots, grid_out[1] = kv_heads x splits).  It runs
- * the same shape validation as fa8_fwd.  Any output pointer may be NULL.
+ * forward's work grid (grid_out[0] = Q-tile slots, grid_out[1] = kv_heads x splits; the
+ * prefill kernel for dv <= 128 is persistent and walks these units with min(units, SMs)
+ * CTAs).  It runs the same shape validation as fa8_fwd.  Any output pointer may be NULL.
  */
 FA8_API fa8_status fa8_fwd_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v,
                                 const fa8_tensor *cu_seqlens_q, const fa8_tensor *cu_seqlens_k,

@@ -77,11 +77,11 @@ def plan(q, k, v, sm=152, **kw):
 
 
 def test_plan_prefill_packs_gqa_rows(lib):
-    # G = 4 q-heads per kv-head -> 32 positions x 4 heads per 128-row tile, two tiles (64
-    # positions) per prefill CTA; 1024 CTAs > 4 per SM, so no split
+    # G = 4 q-heads per kv-head -> 32 positions x 4 heads per 128-row tile (one work unit of
+    # the persistent prefill kernel); 2048 units > 8 per SM, so no split
     splits, ws, grid = plan(*qkv(B=2, Sq=4096, Sk=4096))
     assert splits == 1 and ws == 0
-    assert grid == (2 * (4096 // 64), 8)
+    assert grid == (2 * (4096 // 32), 8)
     # d = 256 (dv > 128) keeps the one-tile kernel: 32 positions per CTA
     assert plan(*qkv(B=2, Sq=4096, Sk=4096, D=256, DV=256))[2] == (2 * (4096 // 32), 8)
 
@@ -119,11 +119,11 @@ def test_plan_depends_on_sm_count_only_through_the_split_heuristic(lib):
 
 
 def test_plan_128_row_kernel_split_cap(lib):
-    # 128-row kernels (Sq x G > 16): at most 64 splits; the prefill kernel (dv <= 128) takes
-    # 2 x 16 positions per CTA, the one-tile kernel (dv > 128) 16
+    # 128-row kernels (Sq x G > 16): at most 64 splits; both the prefill kernel (dv <= 128)
+    # and the one-tile kernel (dv > 128) take 16 positions x 8 heads per tile
     q, k, v = qkv(B=1, Sq=64, Sk=65536, Hq=8, Hkv=1, D=128, DV=128)
     s, _, grid = plan(q, k, v, sm=152)
-    assert grid[0] == 2 and s == 64
+    assert grid[0] == 4 and s == 64
     q, k, v = qkv(B=1, Sq=64, Sk=65536, Hq=8, Hkv=1, D=256, DV=256)
     s, _, grid = plan(q, k, v, sm=152)
     assert grid[0] == 4 and s == 64
@@ -148,9 +148,9 @@ def test_plan_varlen_slots(lib):
     cu = torch.tensor([0, 100, 1000], dtype=torch.int32)
     cuk = torch.tensor([0, 1000, 3000], dtype=torch.int32)
     splits, ws, grid = plan(q, k, v, cu_seqlens_q=cu, cu_seqlens_k=cuk)
-    # 2 x 32 positions per prefill CTA; one extra slot per request for slots that straddle
-    # requests
-    assert grid == ((1000 + 63) // 64 + 2, 4 * splits)
+    # 32 positions (x 4 q-heads) per prefill work unit; one extra slot per request for slots
+    # that straddle requests
+    assert grid == ((1000 + 31) // 32 + 2, 4 * splits)
 
 
 @pytest.mark.parametrize("mutate,status,needle", [
