@@ -31,7 +31,11 @@
 // TMEM (512 columns): S/P of tiles i even / odd at 0 / 128, O_t of tiles i even / odd at 256 /
 // 384.  Hand-offs: S(i) full -> softmax; alpha(i) (4-deep ring) -> correction; P(i) -> MMA;
 // O_t(i) full -> correction; O_t(i) folded -> MMA (PV(i + 2)); per unit, the row's output
-// scale and LSE (4-deep ring) softmax -> correction.  The ring depths follow from the chain
+// scale and LSE (4-deep ring) softmax -> correction.
+// A build with -DFA8_TRACE records clock64() per tile i (< 64) of the first CTAs (debug only):
+// softmax 0 S ready, 1 row max done, 2 P written; producer 3 / 4 K / V load issued; PV issuer
+// 8 waits passed, 9 PV issued; QK issuer 11 PV(i - 2) complete, 10 QK(i) issued; correction 12
+// alpha read, 13 O_t complete, 14 fold done.  The ring depths follow from the chain
 // PV(i) <- fold(i - 2): the softmax can run at most four tiles ahead of the correction.
 #pragma once
 
@@ -446,6 +450,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         ptx::tma_load_4d(dK + c * C::CHUNK_K, &tm_k, BAR(C::B_KF + st), c * C::CW, un.kvh, c2, c3);
                 }
                 issued_k = it + 1;
+                if (lane == 0) FA8_EV(3, it);
                 if (!W.wait_warp(BAR(C::B_VE + st), ph ^ 1u)) { ok = false; break; }
                 if (lane == 0) ptx::mbar_arrive_expect_tx(BAR(C::B_VF + st), (uint32_t)C::V_BYTES);
                 __syncwarp();
@@ -463,6 +468,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         ptx::tma_load_4d(dV + c * C::CHUNK_V, &tm_v, BAR(C::B_VF + st), c * C::CWV, un.kvh, c2, c3);
                 }
                 issued_v = it + 1;
+                if (lane == 0) FA8_EV(4, it);
             }
         }
         if (*abort_flag) {
@@ -499,6 +505,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (is_qk) {
                     // S(i) = Q K_j^T; it overwrites P(i - 2): PV(i - 2) must be complete
                     if (i >= 2 && !W.wait_warp(BAR(C::B_OF + (i & 1)), (((uint32_t)i >> 1) & 1u) ^ 1u)) { ok = false; break; }
+                    if (lane == 0) FA8_EV(11, i);
                     if (j == un.t_beg && !W.wait_warp(BAR(C::B_QF + qb), ((uint32_t)(uidx - 1) >> 1) & 1u)) { ok = false; break; }
                     const int ks = i % C::STAGES;
                     if (!W.wait_warp(BAR(C::B_KF + ks), (uint32_t)(i / C::STAGES) & 1u)) { ok = false; break; }
@@ -517,6 +524,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         if (j + 1 == un.t_end) ptx::tc_commit(BAR(C::B_QE + qb));  // the unit's last QK
                     }
                     __syncwarp();
+                    if (lane == 0) FA8_EV(10, i);
                 } else {
                     // O_t(i) = P(i) V_j (+ P_lo V_j): waits for P(i) and for the fold of O_t(i - 2).
                     // The P_hi MMAs go first; the two-term decision (the mask, or any warp's vote) is
@@ -525,6 +533,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     if (!W.wait_warp(BAR(C::B_VF + vs), (uint32_t)(i / C::STAGES) & 1u)) { ok = false; break; }
                     if (!W.wait_warp(BAR(C::B_PF + (i & 1)), ((uint32_t)i >> 1) & 1u)) { ok = false; break; }
                     if (i >= 2 && !W.wait_warp(BAR(C::B_OE + (i & 1)), (((uint32_t)i >> 1) & 1u) ^ 1u)) { ok = false; break; }
+                    if (lane == 0) FA8_EV(8, i);
                     ptx::tc_fence_after();
                     const uint64_t dv = dv0 + (uint64_t)((vs * C::V_BYTES) >> 4);
                     const uint32_t s_col = tmem + C::TM_S + (uint32_t)(i & 1) * 128u;
@@ -552,6 +561,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                         ptx::tc_commit(BAR(C::B_VE + vs));
                     }
                     __syncwarp();
+                    if (lane == 0) FA8_EV(9, i);
                 }
             }
         }
@@ -587,6 +597,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int j = un.t_beg; j < un.t_end; ++j, ++i) {
             const int k0 = j * kTileN;
             if (!wait_row(BAR(C::B_SF + (i & 1)), ((uint32_t)i >> 1) & 1u)) { ok = false; break; }
+            if (tid == 0) FA8_EV(0, i);
             ptx::tc_fence_after();
             const uint32_t scol = tmem + lane_base + C::TM_S + (uint32_t)(i & 1) * 128u;
             const bool need_mask =
@@ -616,6 +627,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 }
                 ptx::tmem_wait_st();
             }
+            if (tid == 0) FA8_EV(1, i);
             // lazy rescale; alpha(i) to the correction warpgroup
             const float mt = mx * c;
             float alpha = 1.f;
@@ -652,6 +664,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(BAR(C::B_PF + (i & 1)));
+            if (tid == 0) FA8_EV(2, i);
         }
         if (!ok) break;
         // the unit's output scale and LSE for the correction warpgroup; the 2^8 bias cancels
@@ -724,7 +737,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int i = item;
             if (!wait_row(BAR(C::B_AL + (i & 3)), ((uint32_t)i >> 2) & 1u)) { ok = false; break; }
             const float a = alpha_ring[(i & 3) * 128 + r];
+            if (tid == 128) FA8_EV(12, i);
             if (!wait_row(BAR(C::B_OF + (i & 1)), ((uint32_t)i >> 1) & 1u)) { ok = false; break; }
+            if (tid == 128) FA8_EV(13, i);
             ptx::tc_fence_after();
             fold_pass<DV>(tmem + lane_base + C::TM_OT + (uint32_t)(i & 1) * 128u, ptx::f2pack(a, a), o2);
             if (n == nt - 1) {
@@ -737,6 +752,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(BAR(C::B_OE + (i & 1)));
+            if (tid == 128) FA8_EV(14, i);
         }
         if (!ok) break;
         ++uidx;
