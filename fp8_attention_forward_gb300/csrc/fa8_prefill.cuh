@@ -166,14 +166,8 @@ __device__ __forceinline__ int pf_unit_index(const FwdParams &p, int k) {
     return u < p.units ? (int)u : -1;
 }
 
-// The row maximum over the 128 scores held in registers; on tiles that need a mask, columns
-// outside [lo, hi] become -inf first (in registers: the P pass reads the same registers).
-__device__ __forceinline__ float row_max(uint32_t (&u)[128], bool need_mask, int lo, int hi) {
-    if (need_mask) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-            if (i > hi || i < lo) u[i] = __float_as_uint(-INFINITY);
-    }
+// The row maximum over the 128 scores held in registers.
+__device__ __forceinline__ float row_max(const uint32_t (&u)[128]) {
     float m0 = ptx::fmax3(u2f(u[0]), u2f(u[1]), u2f(u[2]));
     float m1 = ptx::fmax3(u2f(u[3]), u2f(u[4]), u2f(u[5]));
     float m2 = ptx::fmax3(u2f(u[6]), u2f(u[7]), u2f(u[8]));
@@ -321,7 +315,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ptx::griddep_wait();
         cap = *p.split_cap;
     }
-    const int PP = p.pos_per_tile;
 
     // ------------------------------------------------------------ shared memory
     uint8_t *misc = smem + C::OFF_MISC;
@@ -606,7 +599,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             if (!need_mask) {
                 uint32_t u[128];
                 tmem_ld128(scol, u);
-                mx = row_max(u, false, 0, 0);
+                mx = row_max(u);
             } else {
                 // tiles with masked columns: 32 at a time, the masked ones written back as -inf
                 // for the P pass (a rolled loop: this path is rare and its code stays small)

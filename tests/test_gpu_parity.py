@@ -354,6 +354,22 @@ def test_split_counts_per_tile_varlen_window():
     assert_parity(case, num_splits=16)
 
 
+@pytest.mark.parametrize("splits", [1, 3], ids=["one_split", "three_splits"])
+def test_persistent_unit_stream(splits):
+    """The prefill kernel is persistent: each CTA walks a list of work units and streams their
+    KV tiles back to back, with a double-buffered Q, 4-deep hand-off rings and the next unit's
+    QKs issued under the current unit's last tiles.  400 varlen sequences of 0-150 tokens
+    (32 positions per unit, mostly one KV tile, some empty) under a causal 64-key window give
+    thousands of short units per CTA, interleaved with units that have no keys in a split
+    (written directly) and splits that do not run."""
+    lens = inputs.uniform_lengths(400, 0, 150, seed=161)
+    case = inputs.make_case(name="unit_stream", B=400, Hq=8, Hkv=2, D=128, DV=128, seqlens_q=lens,
+                            seqlens_k=lens, q_layout="varlen", kv_layout="varlen", causal=True,
+                            window_left=64, sink=True, descale_mode="per_bkv_uniform", seed=161)
+    from parity_util import sample_rows
+    assert_parity(case, rows=sample_rows(case, 800, seed=161), num_splits=splits)
+
+
 def test_split_counts_decode_wide_block_table():
     """Block tables sized for 32k keys, contexts of a few hundred to a few thousand keys: the
     default heuristic launches many splits, the short requests run few of them."""
