@@ -17,7 +17,8 @@
 // so every softmax thread owns one key and holds that key's 16 scores, and the MMAs are
 // 8x smaller than a 128-row tile would make them: the kernel streams K/V at HBM rate
 // instead of spending a 128-row softmax on a handful of rows.  P^T is written to shared
-// memory (K-major, 128-byte swizzle) with plain stores and read by the PV MMA from there.
+// memory MN-major (key t's 16 row bytes at 16 t, no swizzle), one 16-byte store per thread
+// and term, and read by the PV MMA from there.
 //
 // Roles (384 threads): warp 0 TMA producer, warp 1 issues the QK MMAs and warp 2 the PV
 // MMAs (two issuers, so that neither waits behind the other's barriers), warps 4-7 softmax
@@ -53,7 +54,7 @@ struct DecCfg {
     static constexpr int STAGES_FIT = ((CTAS == 2 ? HALF : 232448 - 1024) - FIXED) / (K_BYTES + V_BYTES);
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_P = ((Q_BYTES + 1023) / 1024) * 1024;  // [2 buffers][hi, lo] x 2 KB
+    static constexpr int OFF_P = ((Q_BYTES + 1023) / 1024) * 1024;  // [2 buffers][hi, lo] x 2 KB, MN-major
     static constexpr int OFF_K = OFF_P + 4 * P_BYTES;
     static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
     static constexpr int OFF_MISC = OFF_V + STAGES * V_BYTES;
@@ -62,7 +63,10 @@ struct DecCfg {
     static constexpr uint32_t TM_S = 0;
     static constexpr uint32_t TM_OT = 32;
     static constexpr uint32_t TM_COLS = 128;
-    static constexpr int NA = 4;  // alpha ring (softmax -> fold)
+    // Alpha ring (softmax -> fold).  It needs no "slot free" barrier: the softmax writes the
+    // slot of tile t after waiting for PV(t - 2) to complete, and PV(t - 2) was issued after
+    // the fold of tile t - 4 (which read the slot's previous contents) released its O^T tile.
+    static constexpr int NA = 4;
     // barriers
     static constexpr int B_Q = 0;
     static constexpr int B_KF = 1;
@@ -76,8 +80,7 @@ struct DecCfg {
     static constexpr int B_OF = B_PE + 2;       // 2: O^T tile written
     static constexpr int B_OE = B_OF + 2;       // 2: O^T tile folded
     static constexpr int B_AF = B_OE + 2;       // NA
-    static constexpr int B_AE = B_AF + NA;      // NA
-    static constexpr int B_MX = B_AE + NA;      // 2: tile maxima of the 4 softmax warps written
+    static constexpr int B_MX = B_AF + NA;      // 2: tile maxima of the 4 softmax warps written
     static constexpr int B_SUM = B_MX + 2;      // row-sum shares of the 4 softmax warps written
     static constexpr int B_FIN = B_SUM + 1;     // softmax -> fold: final row scales
     static constexpr int B_DONE = B_FIN + 1;
@@ -87,12 +90,6 @@ struct DecCfg {
     static_assert(NUM_BARS * 8 <= 512, "barrier area");
     static_assert(TM_OT + 2 * NDV * 16 <= TM_COLS, "TMEM budget");
 };
-
-// Byte offset of (row q, key t) in a 16 x 128 K-major tile with the 128-byte swizzle
-// (16-byte chunk index XOR row mod 8), the layout TMA would produce.
-__device__ __forceinline__ uint32_t swz128_offset(int q, int t) {
-    return (uint32_t)(q * 128 + ((((t >> 4) ^ (q & 7))) << 4) + (t & 15));
-}
 
 // Bounded mbarrier waits whose try_wait carries a suspend-time hint: a waiting thread
 // sleeps until the phase completes (woken at once) or the hint expires, instead of
@@ -150,20 +147,28 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
     const int lane = tid & 31;
 
     // ------------------------------------------------------------ tile schedule (batched q)
-    // grid x = kv-head + Hkv * slot (kv-heads fastest), grid y = split: the CTAs of one
-    // request run side by side and share the L2 lines of its pages, and the splits a
-    // request does not use (split >= its split count) come last and exit at once
+    // grid x = kv-head + Hkv * (pair position) with the kv-heads fastest, so that the CTAs of
+    // one (slot, split) pair run side by side and share the L2 lines of its pages.  With a
+    // plan kernel the pair at position x / Hkv + (x-extent / Hkv) * y comes from its list
+    // (longest first, pairs that run no split at its end); otherwise slot = x / Hkv and
+    // split = y, and the splits a request does not use come last and exit at once.
     const int kvh = blockIdx.x % p.Hkv;
-    const int slot = blockIdx.x / p.Hkv;
-    const int b = slot % p.B;
-    const int mb = slot / p.B;
-    const int split = blockIdx.y;
-    const int P = p.pos_per_tile;  // 16 / G positions
+    int slot = blockIdx.x / p.Hkv;
+    int split = blockIdx.y;
     int cap = p.cap_const > 0 ? p.cap_const : (1 << 20);
     if (p.num_splits > 1 && p.cap_const <= 0) {  // chosen by split_plan_kernel, which may still be running
         ptx::griddep_wait();
         cap = *p.split_cap;
+        if (p.unit_order) {
+            const int e = p.unit_order[(long long)blockIdx.y * (gridDim.x / p.Hkv) + slot];
+            if (e < 0) return;
+            slot = e / p.num_splits;
+            split = e - slot * p.num_splits;
+        }
     }
+    const int b = slot % p.B;
+    const int mb = slot / p.B;
+    const int P = p.pos_per_tile;  // 16 / G positions
     const int q_start = b * p.Sq;
     const int Lq = p.Sq;
     int Lk, k_start = 0;
@@ -243,7 +248,6 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         }
         for (int i = 0; i < C::NA; ++i) {
             ptx::mbar_init(BAR(C::B_AF + i), 32);
-            ptx::mbar_init(BAR(C::B_AE + i), 128);
         }
         ptx::mbar_init(BAR(C::B_MX), 128);
         ptx::mbar_init(BAR(C::B_MX + 1), 128);
@@ -344,11 +348,13 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         // ======================================================== MMA issuers: warp 1 issues
         // S^T = K Q^T, warp 2 issues O^T = V^T P^T; each commits its own barriers
         constexpr uint32_t kIdescS = idesc_e4m3(kTileN, kDecRows, false);
-        constexpr uint32_t kIdescO = idesc_e4m3(128, kDecRows, false) | (1u << 15);  // A (V) MN-major
+        constexpr uint32_t kIdescO = idesc_e4m3(128, kDecRows, true) | (1u << 15);  // A (V) and B (P^T) MN-major
         const uint64_t da0 = sdesc(sK, 16, 8 * C::CW, swz_layout(C::CW));
         const uint64_t db0 = sdesc(sQ, 16, 8 * C::CW, swz_layout(C::CW));
         const uint64_t dv0 = sdesc(sV, C::CHUNK_V, 8 * 128, swz_layout(128));
-        const uint64_t dp0 = sdesc(sP, 16, 8 * 128, swz_layout(128));
+        // P^T MN-major without swizzle: core matrices of 8 keys x 16 row bytes (128 B), the
+        // next 8 keys 128 B on; the 16 rows are one core matrix wide, so both strides are 128
+        const uint64_t dp0 = sdesc(sP, 128, 128, 0u);
         const bool leader = ptx::elect_one();
         bool ok = W.wait_warp(BAR(C::B_Q), 0);
         ptx::tc_fence_after();
@@ -387,13 +393,13 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
 #pragma unroll
                     for (int kk = 0; kk < kTileN / 32; ++kk) {
                         const uint64_t a = dv + (uint64_t)((c * C::CHUNK_V + kk * 32 * 128) >> 4);
-                        ptx::mma_f8_ss(ot, a, dp + (uint64_t)((kk * 32) >> 4), kIdescO, kk > 0 ? 1u : 0u);
+                        ptx::mma_f8_ss(ot, a, dp + (uint64_t)((kk * 32 * kDecRows) >> 4), kIdescO, kk > 0 ? 1u : 0u);
                     }
                     if (two_term) {  // + V^T P_lo^T (P_lo buffer follows P_hi)
 #pragma unroll
                         for (int kk = 0; kk < kTileN / 32; ++kk) {
                             const uint64_t a = dv + (uint64_t)((c * C::CHUNK_V + kk * 32 * 128) >> 4);
-                            ptx::mma_f8_ss(ot, a, dp + (uint64_t)((C::P_BYTES + kk * 32) >> 4), kIdescO, 1u);
+                            ptx::mma_f8_ss(ot, a, dp + (uint64_t)((C::P_BYTES + kk * 32 * kDecRows) >> 4), kIdescO, 1u);
                         }
                     }
                 }
@@ -429,10 +435,13 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         const float dqv = p.dq ? p.dq[b * p.dq_sb + kvh * p.dq_sh] : 1.f;
         const float dkv = p.dk ? p.dk[b * p.dk_sb + kvh * p.dk_sh] : 1.f;
         const float c = p.scale_log2 * dqv * dkv;
-        float m_run[kDecRows], rsum[kDecRows];  // identical m_run in every thread
+        // lane q < 16 keeps row q's running max (the same in every warp); every thread keeps
+        // the rows' P biases 8 - m (8 while m = -inf) and its key's share of the row sums
+        float m_lane = -INFINITY;
+        float bias[kDecRows], rsum[kDecRows];
 #pragma unroll
         for (int q = 0; q < kDecRows; ++q) {
-            m_run[q] = -INFINITY;
+            bias[q] = kPBias;
             rsum[q] = 0.f;
         }
         uint8_t *pbase = smem + C::OFF_P;
@@ -468,59 +477,67 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
             }
             ptx::mbar_arrive(BAR(C::B_MX + sb));
             if (!W.wait_warp(BAR(C::B_MX + sb), (uint32_t)(it >> 1) & 1u)) break;
-            float my_alpha = 1.f;  // lane q keeps row q's rescale factor for the hand-off
-#pragma unroll
-            for (int h8 = 0; h8 < kDecRows; h8 += 8) {
-                float4 mv[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mv[i] = ptx::ld_shared_f4(mx_addr + (uint32_t)((h8 + i) * 16));
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int q = h8 + i;
-                    const float mt = fmaxf(fmaxf(mv[i].x, mv[i].y), fmaxf(mv[i].z, mv[i].w)) * c;
-                    if (mt > m_run[q] + kTau) {
-                        const float alpha = ptx::ex2(m_run[q] - mt);
-                        rsum[q] *= alpha;
-                        m_run[q] = mt;
-                        if (lane == q) my_alpha = alpha;
-                    }
+            // lazy rescale, row q in lane q; lane q keeps row q's factor for the hand-off
+            float my_alpha = 1.f;
+            bool resc = false;
+            if (lane < kDecRows) {
+                const float4 mv = ptx::ld_shared_f4(mx_addr + (uint32_t)(lane * 16));
+                const float mt = fmaxf(fmaxf(mv.x, mv.y), fmaxf(mv.z, mv.w)) * c;
+                if (mt > m_lane + kTau) {
+                    my_alpha = ptx::ex2(m_lane - mt);
+                    m_lane = mt;
+                    resc = true;
                 }
             }
-            // warp 4 hands this tile's rescale factors to the fold warps
-            if (sw == 0) {
-                const int as = it % C::NA;
-                if (!W.wait_warp(BAR(C::B_AE + as), ((uint32_t)(it / C::NA) & 1u) ^ 1u)) break;
-                if (lane < kDecRows) ptx::st_shared_f32(ptx::smem_u32(alpha_s) + (uint32_t)((as * kDecRows + lane) * 4), my_alpha);
-                ptx::mbar_arrive(BAR(C::B_AF + as));
+            if (__any_sync(0xffffffffu, resc)) {  // some row's running max moved (rare after the first tiles)
+#pragma unroll
+                for (int q = 0; q < kDecRows; ++q) {
+                    rsum[q] *= __shfl_sync(0xffffffffu, my_alpha, q);
+                    const float mq = __shfl_sync(0xffffffffu, m_lane, q);
+                    bias[q] = kPBias - (mq == -INFINITY ? 0.f : mq);
+                }
             }
             // P^T(it) overwrites P^T(it - 2): wait until PV(it - 2) has read it
             if (!W.wait_warp(BAR(C::B_PE + sb), ((uint32_t)(it >> 1) & 1u) ^ 1u)) break;
-            const uint32_t phi = ptx::smem_u32(pbase) + (uint32_t)(sb * 2 * C::P_BYTES);
-            const uint32_t plo = phi + C::P_BYTES;
-#pragma unroll
-            for (int q = 0; q < kDecRows; q += 2) {
-                const float b0 = kPBias - (m_run[q] == -INFINITY ? 0.f : m_run[q]);
-                const float b1 = kPBias - (m_run[q + 1] == -INFINITY ? 0.f : m_run[q + 1]);
-                const float p0 = ptx::ex2(fmaf(u2f(u[q]), c, b0));
-                const float p1 = ptx::ex2(fmaf(u2f(u[q + 1]), c, b1));
-                rsum[q] += p0;
-                rsum[q + 1] += p1;
-                const uint32_t h = ptx::cvt_e4m3x2(p1, p0);
-                ptx::st_shared_u8(phi + swz128_offset(q, t), h & 0xFFu);
-                ptx::st_shared_u8(phi + swz128_offset(q + 1, t), h >> 8);
-                {  // second E4M3 term on every tile: P_lo = e4m3(p - P_hi)
-                    float q0, q1;
-                    ptx::e4m3x2_to_f32(h, q0, q1);
-                    const uint32_t l = ptx::cvt_e4m3x2(p1 - q1, p0 - q0);
-                    ptx::st_shared_u8(plo + swz128_offset(q, t), l & 0xFFu);
-                    ptx::st_shared_u8(plo + swz128_offset(q + 1, t), l >> 8);
-                }
+            // warp 4 hands this tile's rescale factors to the fold warps (the ring slot is free:
+            // PV(it - 2) has completed, see NA)
+            if (sw == 0) {
+                const int as = it % C::NA;
+                if (lane < kDecRows) ptx::st_shared_f32(ptx::smem_u32(alpha_s) + (uint32_t)((as * kDecRows + lane) * 4), my_alpha);
+                ptx::mbar_arrive(BAR(C::B_AF + as));
             }
+            // key t's P_hi and P_lo bytes of rows 0-15, one 16-byte store each (MN-major P^T)
+            const uint32_t phi = ptx::smem_u32(pbase) + (uint32_t)(sb * 2 * C::P_BYTES) + 16u * (uint32_t)t;
+            const uint64_t c2 = ptx::f2pack(c, c);
+            uint32_t hw[kDecRows / 4], lw[kDecRows / 4];
+#pragma unroll
+            for (int k = 0; k < kDecRows / 4; ++k) {
+                const int q = 4 * k;
+                uint32_t h[2], l[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r0 = q + 2 * e;
+                    float y0, y1;
+                    ptx::f2unpack(ptx::ffma2(ptx::f2pack(u2f(u[r0]), u2f(u[r0 + 1])), c2, ptx::f2pack(bias[r0], bias[r0 + 1])), y0, y1);
+                    const float p0 = ptx::ex2(y0), p1 = ptx::ex2(y1);
+                    rsum[r0] += p0;
+                    rsum[r0 + 1] += p1;
+                    h[e] = ptx::cvt_e4m3x2(p1, p0);
+                    // second E4M3 term on every tile: P_lo = e4m3(p - P_hi)
+                    float q0, q1;
+                    ptx::e4m3x2_to_f32(h[e], q0, q1);
+                    l[e] = ptx::cvt_e4m3x2(p1 - q1, p0 - q0);
+                }
+                hw[k] = ptx::prmt_lo16(h[0], h[1]);
+                lw[k] = ptx::prmt_lo16(l[0], l[1]);
+            }
+            ptx::st_shared_v4(phi, hw[0], hw[1], hw[2], hw[3]);
+            ptx::st_shared_v4(phi + C::P_BYTES, lw[0], lw[1], lw[2], lw[3]);
             ptx::fence_proxy_async_smem();  // the PV MMA reads P^T through the async proxy
             ptx::mbar_arrive(BAR(C::B_PF + sb));
         }
         // finalize: row sums over all keys (each thread holds its keys' share relative to
-        // the common m_run), then per row the output scale and the LSE; the 2^8 bias
+        // the common running max), then per row the output scale and the LSE; the 2^8 bias
         // cancels between O and the row sum and is removed from the LSE
 #pragma unroll
         for (int q = 0; q < kDecRows; ++q) {
@@ -532,10 +549,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         ptx::mbar_arrive(BAR(C::B_SUM));
         if (sw == 0) {
             const bool got = W.wait_warp(BAR(C::B_SUM), 0);
-            float m_q = -INFINITY;
-#pragma unroll
-            for (int q = 0; q < kDecRows; ++q)
-                if (lane == q) m_q = m_run[q];
+            const float m_q = m_lane;
             if (lane < kDecRows) {
                 const int q = lane;
                 const float4 v = *reinterpret_cast<const float4 *>(sum_s + q * 4);
@@ -586,7 +600,6 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
                 alpha[q + 2] = v.z;
                 alpha[q + 3] = v.w;
             }
-            ptx::mbar_arrive(BAR(C::B_AE + as));
             if (!W.wait_warp(BAR(C::B_OF + pb), (uint32_t)(it >> 1) & 1u)) break;
             ptx::tc_fence_after();
 #pragma unroll
