@@ -28,25 +28,10 @@ static __device__ __align__(256) unsigned char g_fa8_static_scratch[FA8_STATIC_S
 namespace fa8 {
 
 __global__ void split_plan_kernel(const __grid_constant__ FwdParams p) {
-    __shared__ int lk[kPlanMaxBatch];
-    __shared__ int hist[kOrderBuckets];
     ptx::griddep_launch_dependents();  // the forward kernel's CTAs may launch meanwhile
-    if (p.unit_order) {  // the key counts, once, for the pair order below
-        for (int b = threadIdx.x; b < p.B; b += 32) {
-            int len = p.kv_mode == 0 ? p.Sk : p.cu_k[b + 1] - p.cu_k[b];
-            // the decode kernel's own validity test of the key count (it reports a bad one)
-            if (p.kv_mode == 1 && (p.cu_k[b] < 0 || p.cu_k[b] + len > p.total_k)) len = -1;
-            if (p.kv_mode == 2 && (long long)len > (long long)p.max_pages * p.page_size) len = -1;
-            lk[b] = len;
-        }
-    }
     const int cap = split_tile_cap(p.B, p.Hkv, p.kv_mode, p.Sk, p.cu_k, p.q_varlen, p.Sq, p.cu_q, p.pos_per_tile,
                                    p.num_splits, p.slots);
     if (threadIdx.x == 0) *p.split_cap = cap;
-    if (p.unit_order) {
-        __syncwarp();
-        decode_unit_order(p, cap, lk, hist);
-    }
 }
 
 __global__ void wait_probe_kernel(unsigned long long timeout_ns, unsigned int *status) {
@@ -395,8 +380,6 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
         const size_t rows = (size_t)p.total_q * p.Hq * splits;
         const size_t o_bytes = (rows * p.DV * sizeof(float) + 255) & ~(size_t)255;
         p.ws_bytes = o_bytes + ((rows * sizeof(float) + 255) & ~(size_t)255) + 256;
-        // the decode kernel's unit order (one int per (slot, split)), before the cap
-        if (p.decode) p.ws_bytes += ((size_t)p.num_slots * splits * sizeof(int) + 255) & ~(size_t)255;
     }
     *pl = p;
     return FA8_SUCCESS;
@@ -730,16 +713,12 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
         p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                                ((rows * pl.DV * sizeof(float) + 255) & ~(size_t)255));
         p.split_cap = reinterpret_cast<int *>(static_cast<char *>(workspace) + pl.ws_bytes - 256);
-        const size_t lse_end = ((rows * pl.DV * sizeof(float) + 255) & ~(size_t)255) +
-                               ((rows * sizeof(float) + 255) & ~(size_t)255);
         // CTAs that run at once: two decode CTAs per SM for (128, 128), one otherwise
         const int per_sm = pl.decode ? fa8::decode_ctas_per_sm(pl.D, pl.DV) : 1;
         p.slots = per_sm * ds->sm_count;
         // when every launched split fits in one wave the finest cap is always the model's
         // choice (split_tile_cap): pass it and skip the plan kernel
         if (pl.base_units * pl.splits <= (long long)p.slots) p.cap_const = 2;
-        // with a plan kernel, the decode CTAs take the (slot, split) pairs longest first
-        if (pl.decode && p.cap_const <= 0 && pl.B <= fa8::kPlanMaxBatch) p.unit_order = reinterpret_cast<int *>(static_cast<char *>(workspace) + lse_end);
     }
     p.timeout_ns = timeout_ns;
     p.status = ds->status;

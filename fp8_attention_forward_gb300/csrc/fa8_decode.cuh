@@ -147,28 +147,20 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
     const int lane = tid & 31;
 
     // ------------------------------------------------------------ tile schedule (batched q)
-    // grid x = kv-head + Hkv * (pair position) with the kv-heads fastest, so that the CTAs of
-    // one (slot, split) pair run side by side and share the L2 lines of its pages.  With a
-    // plan kernel the pair at position x / Hkv + (x-extent / Hkv) * y comes from its list
-    // (longest first, pairs that run no split at its end); otherwise slot = x / Hkv and
-    // split = y, and the splits a request does not use come last and exit at once.
+    // grid x = kv-head + Hkv * slot (kv-heads fastest), grid y = split: the CTAs of one
+    // request run side by side and share the L2 lines of its pages, and the splits a
+    // request does not use (split >= its split count) come last and exit at once
     const int kvh = blockIdx.x % p.Hkv;
-    int slot = blockIdx.x / p.Hkv;
-    int split = blockIdx.y;
+    const int slot = blockIdx.x / p.Hkv;
+    const int b = slot % p.B;
+    const int mb = slot / p.B;
+    const int split = blockIdx.y;
+    const int P = p.pos_per_tile;  // 16 / G positions
     int cap = p.cap_const > 0 ? p.cap_const : (1 << 20);
     if (p.num_splits > 1 && p.cap_const <= 0) {  // chosen by split_plan_kernel, which may still be running
         ptx::griddep_wait();
         cap = *p.split_cap;
-        if (p.unit_order) {
-            const int e = p.unit_order[(long long)blockIdx.y * (gridDim.x / p.Hkv) + slot];
-            if (e < 0) return;
-            slot = e / p.num_splits;
-            split = e - slot * p.num_splits;
-        }
     }
-    const int b = slot % p.B;
-    const int mb = slot / p.B;
-    const int P = p.pos_per_tile;  // 16 / G positions
     const int q_start = b * p.Sq;
     const int Lq = p.Sq;
     int Lk, k_start = 0;

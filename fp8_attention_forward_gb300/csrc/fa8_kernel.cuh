@@ -132,10 +132,6 @@ struct FwdParams {
     int *split_cap;
     int cap_const;
     int units;  // work units of the persistent prefill kernel (slot, kv-head, split)
-    // decode kernel with a plan kernel: the (slot, split) pairs, longest first, that its
-    // CTAs take in launch order (split_plan_kernel writes it; -1 past the last one); null:
-    // the grid coordinates name the pair directly
-    int *unit_order;
 };
 
 struct CombineParams {
@@ -429,77 +425,8 @@ __device__ __forceinline__ int split_tile_cap(int B, int Hkv, int kv_mode, int S
     return best_cap;
 }
 
-// The order in which the decode kernel's CTAs take the (slot, split) pairs of a launch with
-// a plan kernel: longest first (list scheduling by decreasing processing time), so that the
-// last CTAs to start are short ones and the launch ends with little tail.  A pair's length is
-// its KV tile count, split_range's n_tiles under the launch's cap, exactly as the decode
-// kernel derives it; pairs of splits a tile does not run are left out, and the pairs of
-// equal length keep their index order.  Pair e = slot * num_splits + split, slot = b +
-// B * mb (batched q).  The whole warp calls it; lk holds the requests' key counts (B
-// entries, shared memory) and hist kOrderBuckets ints of shared memory.  The list has
-// B * mblocks * num_splits entries, -1 past the last pair.
-constexpr int kOrderBuckets = 1024;
-constexpr int kPlanMaxBatch = 4096;  // requests whose key counts the plan kernel stages in shared memory
-__device__ __forceinline__ int decode_pair_tiles(const FwdParams &p, const int *lk, int e, int cap) {
-    const int slot = e / p.num_splits, split = e - slot * p.num_splits;
-    const int b = slot % p.B, mb = slot / p.B;
-    const int pos0 = mb * p.pos_per_tile;
-    if (pos0 >= p.Sq) return -1;
-    const int Lk = lk[b];
-    if (Lk < 0) return split == 0 ? 0 : -1;  // a bad key count: split 0 runs and reports it
-    const int pos_last = min(pos0 + p.pos_per_tile, p.Sq) - 1;
-    const SplitRange sr =
-        split_range(p.Sq, Lk, pos0, pos_last, p.causal, p.window_left, p.num_splits, cap, split);
-    if (split >= sr.eff) return -1;
-    return min(sr.n_tiles, kOrderBuckets - 1);
-}
-__device__ __forceinline__ void decode_unit_order(const FwdParams &p, int cap, const int *lk, int *hist) {
-    const int lane = threadIdx.x & 31;
-    const int n = p.B * p.mblocks_per_batch * p.num_splits;
-    for (int i = lane; i < kOrderBuckets; i += 32) hist[i] = 0;
-    __syncwarp();
-    for (int e = lane; e < n; e += 32) {
-        const int t = decode_pair_tiles(p, lk, e, cap);
-        if (t >= 0) atomicAdd(&hist[kOrderBuckets - 1 - t], 1);
-    }
-    __syncwarp();
-    // bucket starts: exclusive prefix sum, lane l owning buckets [32 l, 32 l + 32)
-    constexpr int kPerLane = kOrderBuckets / 32;
-    int own = 0;
-    for (int i = 0; i < kPerLane; ++i) own += hist[kPerLane * lane + i];
-    int inc = own;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, inc, 31);
-    int start = inc - own;
-    for (int i = 0; i < kPerLane; ++i) {
-        const int c = hist[kPerLane * lane + i];
-        hist[kPerLane * lane + i] = start;
-        start += c;
-    }
-    __syncwarp();
-    // stable scatter, 32 pairs at a time: lanes of one bucket take consecutive places
-    const unsigned lower = (1u << lane) - 1u;
-    for (int e0 = 0; e0 < n; e0 += 32) {
-        const int e = e0 + lane;
-        const int t = e < n ? decode_pair_tiles(p, lk, e, cap) : -1;
-        const int key = t >= 0 ? kOrderBuckets - 1 - t : -1 - lane;  // unmatched key for a lane without a pair
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        const int pos = t >= 0 ? hist[key] + __popc(peers & lower) : 0;
-        __syncwarp();
-        if (t >= 0 && (peers & lower) == 0u) hist[key] += __popc(peers);
-        __syncwarp();
-        if (t >= 0) p.unit_order[pos] = e;
-    }
-    for (int i = total + lane; i < n; i += 32) p.unit_order[i] = -1;
-}
-
 // One warp: chooses the launch's split cap (split_tile_cap) before the forward kernel runs
-// and leaves it in the workspace for the forward and combine kernels, with the decode
-// kernel's pair order (decode_unit_order) when that kernel takes one.
+// and leaves it in the workspace for the forward and combine kernels.
 __global__ void split_plan_kernel(const __grid_constant__ FwdParams p);
 
 // Maps a varlen grid slot to (request, slot within the request): the slots enumerate each

@@ -98,9 +98,8 @@ def test_plan_decode_splits_and_workspace(lib):
     assert splits == 3
     rows = B * Hq * splits
     o_bytes = (rows * D * 4 + 255) // 256 * 256
-    # partials, the decode CTAs' (request, split) order (one int per pair), then 256 bytes
-    # where the forward kernel records its split cap
-    assert ws == o_bytes + (rows * 4 + 255) // 256 * 256 + (B * splits * 4 + 255) // 256 * 256 + 256
+    # partials, then 256 bytes where the forward kernel records its split cap
+    assert ws == o_bytes + (rows * 4 + 255) // 256 * 256 + 256
     assert grid == (B, Hkv * splits)
     # an explicit split count is capped by the number of key tiles
     s2, _, _ = plan(q, kp, kp, cu_seqlens_k=cu, block_table=bt, page_size=16, num_splits=4096)

@@ -135,26 +135,6 @@ def _model_cap(lens, Hkv, n, slots, lens_q=None, P=1):
     return best[1]
 
 
-def _model_order(lens, n, cap):
-    """The decode kernel's pair order for one-token requests (restated on the host): pairs
-    e = request * n + split whose split runs tiles, longest first, then -1."""
-    import math
-    keyed = []
-    for e in range(len(lens) * n):
-        b, s = divmod(e, n)
-        nt = math.ceil(lens[b] / 128)
-        if nt == 0:
-            if s == 0:
-                keyed.append((0, e))
-            continue
-        eff = max(1, min(n, math.ceil(nt / cap)))
-        per = math.ceil(nt / eff)
-        if s < eff:
-            keyed.append((min(1023, max(0, min(nt, s * per + per) - s * per)), e))
-    keyed.sort(key=lambda x: (-x[0], x[1]))
-    return [e for _, e in keyed] + [-1] * (len(lens) * n - len(keyed))
-
-
 @pytest.mark.parametrize("B,ctx,hq,hkv", [(32, 2048, 32, 8), (16, 16384, 32, 8), (64, 4096, 16, 2),
                                            (8, 32768, 16, 2), (24, None, 16, 2)])
 def test_split_cap_follows_the_key_counts(B, ctx, hq, hkv):
@@ -174,12 +154,6 @@ def test_split_cap_follows_the_key_counts(B, ctx, hq, hkv):
     run_gpu(c, workspace=ws)
     cap = int(ws[ws_bytes - 256:ws_bytes - 252].view(torch.int32).item())
     assert cap == _model_cap(lens, hkv, splits, slots)
-    # the decode CTAs' (request, split) order, just below the cap: the pairs that run, by
-    # decreasing tile count, ties in index order, then -1
-    n = B * splits
-    at = ws_bytes - 256 - ((4 * n + 255) // 256) * 256
-    order = ws[at:at + 4 * n].view(torch.int32).cpu().tolist()
-    assert order == _model_order(lens, splits, cap)
     rows = [(i, h) for i in range(B) for h in (0, hq - 1)]
     assert_parity(case, rows=rows)
 
