@@ -47,7 +47,7 @@ METRIC = "FP8 attn fwd TFLOP/s (prefill) & decode HBM GB/s; % of GB300 roofline"
 PROFILED_TRAFFIC = {
     "prefill": {"kernel": "prefill_kernel<128,128>", "bytes": 67.26e6,
                 "sources": ["fa8_prefill.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "96446e6aae9f27be"},
-    "decode": {"kernel": "decode_kernel<128,128>", "bytes": 2073.29e6,
+    "decode": {"kernel": "decode_kernel<128,128,8>", "bytes": 2073.29e6,
                "sources": ["fa8_decode.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "8da8ef71a72461c0"},
 }
 
@@ -195,7 +195,7 @@ def bench_case(case, steps, warmup, flush, fa8, num_splits=0, graph=False):
     if splits > 1:
         sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
         name = _decode_kernel_name(case)
-        per_sm = 2 if name.startswith("decode_kernel<128,128>") else 1
+        per_sm = 2 if name.startswith("decode_kernel<128,128,") else 1
         g = case.Hq // case.Hkv
         # positions per work unit: a 16-row decode tile or a 128-row tile
         pos = 16 // g if name.startswith("decode_kernel") else 128 // g
@@ -365,13 +365,13 @@ def cpu_baseline_for(case, bound, budget_s, threads):
 
 def _decode_kernel_name(case):
     """The kernel include/fa8.h documents for this shape: the few-rows decode kernel when
-    query positions x (Hq / Hkv) <= 16 with Hq / Hkv dividing 16 (batched q, dv % 128 = 0);
-    otherwise the persistent prefill kernel for dv <= 128 and the one-tile kernel above."""
+    query positions x (Hq / Hkv) <= 16 with Hq / Hkv dividing 16 (batched q, dv % 128 = 0),
+    carrying 8 rows when that product is at most 8, else 16; otherwise the persistent prefill kernel for dv <= 128 and the one-tile kernel above."""
     g = case.Hq // case.Hkv
     sq = case.seqlens_q[0]
     few = case.q_layout == "batched" and case.DV % 128 == 0 and 16 % g == 0 and sq * g <= 16
     if few:
-        return f"decode_kernel<{case.D},{case.DV}>"
+        return f"decode_kernel<{case.D},{case.DV},{8 if sq * g <= 8 else 16}>"
     return f"prefill_kernel<{case.D},{case.DV}>" if case.DV <= 128 else f"fwd_kernel<{case.D},{case.DV}>"
 
 

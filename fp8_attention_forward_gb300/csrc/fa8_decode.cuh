@@ -134,7 +134,10 @@ __device__ __forceinline__ float redux_max(float v) {
     return r;
 }
 
-template <int D, int DV>
+// R: the rows the softmax and fold carry (8 when a tile holds at most 8 real rows, as in
+// one-token decode with up to 8 q-heads per kv-head; 16 otherwise).  The MMAs always run N = 16:
+// P^T rows R..15 stay zero and the O^T columns beyond R are never read.
+template <int D, int DV, int R>
 __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
     decode_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -248,6 +251,11 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         ptx::mbar_init(BAR(C::B_DONE), 2);
         *abort_flag = 0;
         ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (R < kDecRows) {  // P^T rows the softmax never writes read as zero by the PV MMA
+        for (int i = tid; i < 4 * C::P_BYTES / 16; i += kDecThreads)
+            ptx::st_shared_v4(sP + 16u * (uint32_t)i, 0u, 0u, 0u, 0u);
         ptx::fence_proxy_async_smem();
     }
     if (warp == 0 && lane == 0) {
@@ -430,9 +438,9 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         // lane q < 16 keeps row q's running max (the same in every warp); every thread keeps
         // the rows' P biases 8 - m (8 while m = -inf) and its key's share of the row sums
         float m_lane = -INFINITY;
-        float bias[kDecRows], rsum[kDecRows];
+        float bias[R], rsum[R];
 #pragma unroll
-        for (int q = 0; q < kDecRows; ++q) {
+        for (int q = 0; q < R; ++q) {
             bias[q] = kPBias;
             rsum[q] = 0.f;
         }
@@ -453,7 +461,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
             if (need_mask) {
                 const int kg = k0 + t;
 #pragma unroll
-                for (int q = 0; q < kDecRows; ++q) {
+                for (int q = 0; q < R; ++q) {
                     const int pos = row_pos(q);
                     const int hi = row_ok(q) ? (p.causal ? min(Lk - 1, pos + delta) : Lk - 1) : -1;
                     const int lo = p.window_left >= 0 ? max(0, pos + delta - p.window_left) : 0;
@@ -463,7 +471,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
             // tile max of every row over the 128 keys: warp reduction, then across the 4 warps
             const uint32_t mx_addr = ptx::smem_u32(mx_s) + (uint32_t)(sb * kDecRows * 4 * 4);
 #pragma unroll
-            for (int q = 0; q < kDecRows; ++q) {
+            for (int q = 0; q < R; ++q) {
                 const float m = redux_max(u2f(u[q]));
                 if (lane == q) ptx::st_shared_f32(mx_addr + (uint32_t)((q * 4 + sw) * 4), m);
             }
@@ -472,7 +480,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
             // lazy rescale, row q in lane q; lane q keeps row q's factor for the hand-off
             float my_alpha = 1.f;
             bool resc = false;
-            if (lane < kDecRows) {
+            if (lane < R) {
                 const float4 mv = ptx::ld_shared_f4(mx_addr + (uint32_t)(lane * 16));
                 const float mt = fmaxf(fmaxf(mv.x, mv.y), fmaxf(mv.z, mv.w)) * c;
                 if (mt > m_lane + kTau) {
@@ -483,7 +491,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
             }
             if (__any_sync(0xffffffffu, resc)) {  // some row's running max moved (rare after the first tiles)
 #pragma unroll
-                for (int q = 0; q < kDecRows; ++q) {
+                for (int q = 0; q < R; ++q) {
                     rsum[q] *= __shfl_sync(0xffffffffu, my_alpha, q);
                     const float mq = __shfl_sync(0xffffffffu, m_lane, q);
                     bias[q] = kPBias - (mq == -INFINITY ? 0.f : mq);
@@ -495,15 +503,15 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
             // PV(it - 2) has completed, see NA)
             if (sw == 0) {
                 const int as = it % C::NA;
-                if (lane < kDecRows) ptx::st_shared_f32(ptx::smem_u32(alpha_s) + (uint32_t)((as * kDecRows + lane) * 4), my_alpha);
+                if (lane < R) ptx::st_shared_f32(ptx::smem_u32(alpha_s) + (uint32_t)((as * kDecRows + lane) * 4), my_alpha);
                 ptx::mbar_arrive(BAR(C::B_AF + as));
             }
             // key t's P_hi and P_lo bytes of rows 0-15, one 16-byte store each (MN-major P^T)
             const uint32_t phi = ptx::smem_u32(pbase) + (uint32_t)(sb * 2 * C::P_BYTES) + 16u * (uint32_t)t;
             const uint64_t c2 = ptx::f2pack(c, c);
-            uint32_t hw[kDecRows / 4], lw[kDecRows / 4];
+            uint32_t hw[R / 4], lw[R / 4];
 #pragma unroll
-            for (int k = 0; k < kDecRows / 4; ++k) {
+            for (int k = 0; k < R / 4; ++k) {
                 const int q = 4 * k;
                 uint32_t h[2], l[2];
 #pragma unroll
@@ -523,8 +531,14 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
                 hw[k] = ptx::prmt_lo16(h[0], h[1]);
                 lw[k] = ptx::prmt_lo16(l[0], l[1]);
             }
-            ptx::st_shared_v4(phi, hw[0], hw[1], hw[2], hw[3]);
-            ptx::st_shared_v4(phi + C::P_BYTES, lw[0], lw[1], lw[2], lw[3]);
+            if constexpr (R == 16) {
+                ptx::st_shared_v4(phi, hw[0], hw[1], hw[2], hw[3]);
+                ptx::st_shared_v4(phi + C::P_BYTES, lw[0], lw[1], lw[2], lw[3]);
+            } else {
+                static_assert(R == 8, "decode kernel: 8 or 16 rows");
+                ptx::st_shared_v2(phi, hw[0], hw[1]);
+                ptx::st_shared_v2(phi + C::P_BYTES, lw[0], lw[1]);
+            }
             ptx::fence_proxy_async_smem();  // the PV MMA reads P^T through the async proxy
             ptx::mbar_arrive(BAR(C::B_PF + sb));
         }
@@ -532,7 +546,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         // the common running max), then per row the output scale and the LSE; the 2^8 bias
         // cancels between O and the row sum and is removed from the LSE
 #pragma unroll
-        for (int q = 0; q < kDecRows; ++q) {
+        for (int q = 0; q < R; ++q) {
             float v = rsum[q];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -542,7 +556,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         if (sw == 0) {
             const bool got = W.wait_warp(BAR(C::B_SUM), 0);
             const float m_q = m_lane;
-            if (lane < kDecRows) {
+            if (lane < R) {
                 const int q = lane;
                 const float4 v = *reinterpret_cast<const float4 *>(sum_s + q * 4);
                 const float rs_q = got ? (v.x + v.y) + (v.z + v.w) : 0.f;
@@ -575,17 +589,17 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         // ======================================================== fold + epilogue (thread = dv row)
         const int m = tid - 256;
         const uint32_t lane_base = (uint32_t)((warp - 8) * 32) << 16;
-        float o[C::NDV][kDecRows];
+        float o[C::NDV][R];
 #pragma unroll
         for (int cc = 0; cc < C::NDV; ++cc)
 #pragma unroll
-            for (int q = 0; q < kDecRows; ++q) o[cc][q] = 0.f;
+            for (int q = 0; q < R; ++q) o[cc][q] = 0.f;
         for (int it = 0; it < n_tiles; ++it) {
             const int as = it % C::NA, pb = it & 1;
             if (!W.wait_warp(BAR(C::B_AF + as), (uint32_t)(it / C::NA) & 1u)) break;
-            float alpha[kDecRows];
+            float alpha[R];
 #pragma unroll
-            for (int q = 0; q < kDecRows; q += 4) {
+            for (int q = 0; q < R; q += 4) {
                 const float4 v = *reinterpret_cast<const float4 *>(alpha_s + as * kDecRows + q);
                 alpha[q] = v.x;
                 alpha[q + 1] = v.y;
@@ -601,14 +615,14 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
                 ptx::tmem_wait_ld();
                 ptx::reg_fence16(u);
 #pragma unroll
-                for (int q = 0; q < kDecRows; ++q) o[cc][q] = fmaf(o[cc][q], alpha[q], u2f(u[q]));
+                for (int q = 0; q < R; ++q) o[cc][q] = fmaf(o[cc][q], alpha[q], u2f(u[q]));
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(BAR(C::B_OE + pb));
         }
         const bool fin = W.wait_warp(BAR(C::B_FIN), 0);
 #pragma unroll
-        for (int q = 0; q < kDecRows; ++q) {
+        for (int q = 0; q < R; ++q) {
             if (!row_ok(q)) continue;
             const float sc = fin ? scale_s[q] : 0.f;
             const int pos = row_pos(q), hq = kvh * p.G + q % p.G, tok = q_start + pos;

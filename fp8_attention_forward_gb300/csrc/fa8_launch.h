@@ -107,18 +107,26 @@ inline cudaError_t launch_after_plan(K *kernel, const FwdParams &p, const CUtens
         return launch_after_plan(prefill_kernel<D_, DV_>, p, tq, tk, tv, grid, kPfThreads, smem, stream); \
     }
 
-// Defines launch_decode<D, DV> (the few-rows kernel, dv a multiple of 128).
+// The few-rows kernel carrying R rows (see decode_kernel).
+template <int D, int DV, int R>
+inline cudaError_t launch_decode_rows(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                                      const CUtensorMap &tv, dim3 grid, cudaStream_t stream) {
+    constexpr int smem = DecCfg<D, DV>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, DV, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_after_plan(decode_kernel<D, DV, R>, p, tq, tk, tv, grid, kDecThreads, smem, stream);
+}
+
+// Defines launch_decode<D, DV> (the few-rows kernel, dv a multiple of 128): 8 carried rows
+// when a tile's real rows (query positions in the tile x q-heads per kv-head) fit in 8.
 #define FA8_DEFINE_DECODE(D_, DV_)                                                           \
     template <>                                                                              \
     cudaError_t launch_decode<D_, DV_>(const FwdParams &p, const CUtensorMap &tq,            \
                                        const CUtensorMap &tk, const CUtensorMap &tv,         \
                                        dim3 grid, cudaStream_t stream) {                     \
-        constexpr int smem = DecCfg<D_, DV_>::SMEM_BYTES;                                    \
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D_, DV_>,                         \
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,    \
-                                             smem);                                          \
-        if (e != cudaSuccess) return e;                                                      \
-        return launch_after_plan(decode_kernel<D_, DV_>, p, tq, tk, tv, grid, kDecThreads, smem, stream); \
+        const int rows = (p.Sq < p.pos_per_tile ? p.Sq : p.pos_per_tile) * p.G;              \
+        return rows <= 8 ? launch_decode_rows<D_, DV_, 8>(p, tq, tk, tv, grid, stream)       \
+                         : launch_decode_rows<D_, DV_, 16>(p, tq, tk, tv, grid, stream);     \
     }
 
 }  // namespace fa8
