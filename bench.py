@@ -366,12 +366,12 @@ def cpu_baseline_for(case, bound, budget_s, threads):
 def _decode_kernel_name(case):
     """The kernel include/fa8.h documents for this shape: the few-rows decode kernel when
     query positions x (Hq / Hkv) <= 16 with Hq / Hkv dividing 16 (batched q, dv % 128 = 0),
-    carrying 8 rows when that product is at most 8, else 16; otherwise the persistent prefill kernel for dv <= 128 and the one-tile kernel above."""
+    carrying 4 or 8 rows when that product is at most 4 or 8, else 16; otherwise the persistent prefill kernel for dv <= 128 and the one-tile kernel above."""
     g = case.Hq // case.Hkv
     sq = case.seqlens_q[0]
     few = case.q_layout == "batched" and case.DV % 128 == 0 and 16 % g == 0 and sq * g <= 16
     if few:
-        return f"decode_kernel<{case.D},{case.DV},{8 if sq * g <= 8 else 16}>"
+        return f"decode_kernel<{case.D},{case.DV},{4 if sq * g <= 4 else (8 if sq * g <= 8 else 16)}>"
     return f"prefill_kernel<{case.D},{case.DV}>" if case.DV <= 128 else f"fwd_kernel<{case.D},{case.DV}>"
 
 

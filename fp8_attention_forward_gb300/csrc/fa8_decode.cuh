@@ -134,9 +134,9 @@ __device__ __forceinline__ float redux_max(float v) {
     return r;
 }
 
-// R: the rows the softmax and fold carry (8 when a tile holds at most 8 real rows, as in
-// one-token decode with up to 8 q-heads per kv-head; 16 otherwise).  The MMAs always run N = 16:
-// P^T rows R..15 stay zero and the O^T columns beyond R are never read.
+// R: the rows the softmax and fold carry (4 or 8 when a tile holds at most that many real
+// rows, as in one-token decode with 4 or 8 q-heads per kv-head; 16 otherwise).  The MMAs
+// always run N = 16: P^T rows R..15 stay zero and the O^T columns beyond R are never read.
 template <int D, int DV, int R>
 __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
     decode_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -534,10 +534,13 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
             if constexpr (R == 16) {
                 ptx::st_shared_v4(phi, hw[0], hw[1], hw[2], hw[3]);
                 ptx::st_shared_v4(phi + C::P_BYTES, lw[0], lw[1], lw[2], lw[3]);
-            } else {
-                static_assert(R == 8, "decode kernel: 8 or 16 rows");
+            } else if constexpr (R == 8) {
                 ptx::st_shared_v2(phi, hw[0], hw[1]);
                 ptx::st_shared_v2(phi + C::P_BYTES, lw[0], lw[1]);
+            } else {
+                static_assert(R == 4, "decode kernel: 4, 8 or 16 rows");
+                ptx::st_shared_u32(phi, hw[0]);
+                ptx::st_shared_u32(phi + C::P_BYTES, lw[0]);
             }
             ptx::fence_proxy_async_smem();  // the PV MMA reads P^T through the async proxy
             ptx::mbar_arrive(BAR(C::B_PF + sb));

@@ -117,16 +117,17 @@ inline cudaError_t launch_decode_rows(const FwdParams &p, const CUtensorMap &tq,
     return launch_after_plan(decode_kernel<D, DV, R>, p, tq, tk, tv, grid, kDecThreads, smem, stream);
 }
 
-// Defines launch_decode<D, DV> (the few-rows kernel, dv a multiple of 128): 8 carried rows
-// when a tile's real rows (query positions in the tile x q-heads per kv-head) fit in 8.
+// Defines launch_decode<D, DV> (the few-rows kernel, dv a multiple of 128): 4 or 8 carried
+// rows when a tile's real rows (query positions in the tile x q-heads per kv-head) fit.
 #define FA8_DEFINE_DECODE(D_, DV_)                                                           \
     template <>                                                                              \
     cudaError_t launch_decode<D_, DV_>(const FwdParams &p, const CUtensorMap &tq,            \
                                        const CUtensorMap &tk, const CUtensorMap &tv,         \
                                        dim3 grid, cudaStream_t stream) {                     \
         const int rows = (p.Sq < p.pos_per_tile ? p.Sq : p.pos_per_tile) * p.G;              \
-        return rows <= 8 ? launch_decode_rows<D_, DV_, 8>(p, tq, tk, tv, grid, stream)       \
-                         : launch_decode_rows<D_, DV_, 16>(p, tq, tk, tv, grid, stream);     \
+        return rows <= 4   ? launch_decode_rows<D_, DV_, 4>(p, tq, tk, tv, grid, stream)     \
+               : rows <= 8 ? launch_decode_rows<D_, DV_, 8>(p, tq, tk, tv, grid, stream)     \
+                           : launch_decode_rows<D_, DV_, 16>(p, tq, tk, tv, grid, stream);   \
     }
 
 }  // namespace fa8
