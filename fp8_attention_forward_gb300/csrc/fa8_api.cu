@@ -216,9 +216,48 @@ struct Plan {
     int prefill = 0;  // launch prefill_kernel (persistent, one 128-row Q tile per work unit, dv <= 128)
     long long base_units = 0;  // (tile of query rows, kv-head) pairs, before splitting
     long long units = 0;       // (slot, kv-head, split) work units
+    int cap = 0;  // split cap chosen on the host (dense K/V, batched q); 0: as the launch decides
 };
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The split cap for dense K/V with batched q: every request has the same key and query
+// counts, so the host knows all that split_plan_kernel would read.  The same model as
+// fa8::split_tile_cap (fixed cost F per unit, tail weight beta, candidates 2, 4, ..., 512 and
+// the finest cap the launch allows), plus one candidate the device does not try: the finest
+// cap whose units all run in one wave (the powers of two can miss it by up to 2x, leaving SMs
+// idle for the whole launch).
+int uniform_split_cap(int B, int Hkv, int Sk, int Sq, int P, int n, int slots) {
+    const long long t = Sk > 0 ? (Sk + 127) / 128 : 0;
+    const long long mb = Sq > 0 ? (Sq + P - 1) / P : 0;
+    const int t_fine = (int)std::max<long long>(2, (t + n - 1) / n);
+    const float tiles = (float)(B * t * mb);
+    auto cost = [&](long long T) {
+        const float units = (float)((long long)B * mb * ((t + T - 1) / T)) * (float)Hkv;
+        const float tail = fa8::kFixedTiles + (float)std::min<long long>(T, t);
+        return units <= (float)slots ? tail
+                                     : (fa8::kFixedTiles * units + tiles * (float)Hkv) * (1.f / (float)slots) +
+                                           fa8::kTailWeight * tail;
+    };
+    int best_cap = t_fine;
+    float best = 3.0e38f;
+    for (int c = 0; c < 10; ++c) {
+        const int T = c < 9 ? (2 << c) : t_fine;
+        if (T < t_fine) continue;
+        const float m = cost(T);
+        if (m < best) {
+            best = m;
+            best_cap = T;
+        }
+    }
+    const long long per_split = (long long)B * mb * Hkv;  // units per split of every request
+    if (t > 0 && per_split > 0 && per_split <= slots) {
+        const long long k = slots / per_split;  // splits per request that still fit one wave
+        const long long T = std::max<long long>(t_fine, (t + k - 1) / k);
+        if (cost(T) < best) best_cap = (int)T;
+    }
+    return best_cap;
+}
 
 fa8_status check_int_vec(const fa8_tensor *t, const char *name, long long n) {
     if (t->dtype != FA8_DTYPE_I32) return fail(FA8_ERR_INVALID_ARG, "%s must be int32", name);
@@ -369,6 +408,20 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
         }
     } else {
         splits = std::min(num_splits, max_tiles);
+    }
+    // Dense K/V with batched q: every request has the same key and query counts, so the host
+    // can choose the split cap itself (uniform_split_cap) instead of a plan kernel, and with
+    // the heuristic's split count launch only the splits that run.
+    if (splits > 1 && p.kv_mode == 0 && !p.q_varlen && p.Sk > 0) {
+        const int per_sm = p.decode ? fa8::decode_ctas_per_sm(p.D, p.DV) : 1;
+        const int slots = per_sm * sm_count;
+        if (base_ctas * splits > (long long)slots) {
+            p.cap = uniform_split_cap(p.B, p.Hkv, p.Sk, p.Sq, p.P, splits, slots);
+            if (num_splits == 0) {
+                const long long t = (p.Sk + 127) / 128;
+                splits = (int)std::max<long long>(1, std::min<long long>(splits, (t + p.cap - 1) / p.cap));
+            }
+        }
     }
     if ((long long)splits * p.Hkv > 65535) return fail(FA8_ERR_UNSUPPORTED, "kv_heads x splits exceeds the grid limit");
     p.splits = splits;
@@ -718,7 +771,8 @@ fa8_status fa8_fwd(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor *v
         p.slots = per_sm * ds->sm_count;
         // when every launched split fits in one wave the finest cap is always the model's
         // choice (split_tile_cap): pass it and skip the plan kernel
-        if (pl.base_units * pl.splits <= (long long)p.slots) p.cap_const = 2;
+        if (pl.cap > 0) p.cap_const = pl.cap;  // chosen with the plan (dense K/V, batched q)
+        else if (pl.base_units * pl.splits <= (long long)p.slots) p.cap_const = 2;
     }
     p.timeout_ns = timeout_ns;
     p.status = ds->status;
