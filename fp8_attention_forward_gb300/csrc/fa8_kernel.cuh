@@ -382,21 +382,26 @@ __device__ __forceinline__ int split_tile_cap(int B, int Hkv, int kv_mode, int S
     }
     auto add_t = [&](int lk) { t_max = max(t_max, lk > 0 ? (lk + kTileN - 1) / kTileN : 0); };
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) add_t(lks[i]);
+    for (int i = 0; i < kPer; ++i)
+        if (32 * i < B) add_t(lks[i]);  // (slots past the batch skipped by the whole warp)
     for (int b = lane + 32 * kPer; b < B; b += 32) add_t(kv_mode == 0 ? Sk : cu_k[b + 1] - cu_k[b]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t_max = max(t_max, __shfl_xor_sync(0xffffffffu, t_max, o));
     const int t_fine = max(2, (t_max + num_splits - 1) / num_splits);
     auto cand = [&](int c) { return c < NC - 1 ? (2 << c) : t_fine; };
+    // query tiles per request: one division for batched q, where every request has Sq rows
+    const unsigned int mb_batched = Sq > 0 ? (unsigned int)(Sq + pos_per_tile - 1) / pos_per_tile : 0u;
     auto add_units = [&](int lk, int lq) {
         const unsigned int t = lk > 0 ? (unsigned int)(lk + kTileN - 1) / kTileN : 0u;
-        const unsigned int mb = lq > 0 ? (unsigned int)(lq + pos_per_tile - 1) / pos_per_tile : 0u;
+        const unsigned int mb = !q_varlen ? (lq > 0 ? mb_batched : 0u)
+                                          : (lq > 0 ? (unsigned int)(lq + pos_per_tile - 1) / pos_per_tile : 0u);
         tiles += t * mb;
 #pragma unroll
         for (int c = 0; c < NC; ++c) units[c] += mb * ((t + (unsigned int)cand(c) - 1u) / (unsigned int)cand(c));
     };
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) add_units(lks[i], lqs[i]);
+    for (int i = 0; i < kPer; ++i)
+        if (32 * i < B) add_units(lks[i], lqs[i]);
     for (int b = lane + 32 * kPer; b < B; b += 32)
         add_units(kv_mode == 0 ? Sk : cu_k[b + 1] - cu_k[b], q_varlen ? cu_q[b + 1] - cu_q[b] : Sq);
 #pragma unroll
