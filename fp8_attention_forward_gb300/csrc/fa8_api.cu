@@ -398,10 +398,14 @@ fa8_status make_plan(const fa8_tensor *q, const fa8_tensor *k, const fa8_tensor 
         // (the decode kernel, cheaper per CTA, may split up to 128 ways)
         const long long target = 8LL * sm_count;
         const long long cap = p.decode ? 128 : 64;
+        // few (tile, kv-head) pairs: as many splits as fit in one wave of CTAs.  With every
+        // launched split in one wave the finest cap is the model's answer whatever the key
+        // counts (split_tile_cap), so the launch passes it and runs no plan kernel.
+        const long long one_wave = (long long)(p.decode ? fa8::decode_ctas_per_sm(p.D, p.DV) : 1) * sm_count;
         if (base_ctas >= target || max_tiles < 4) {
             splits = 1;
         } else {
-            long long s = (target + base_ctas - 1) / base_ctas;
+            long long s = 2 * base_ctas <= one_wave ? one_wave / base_ctas : (target + base_ctas - 1) / base_ctas;
             s = std::min<long long>(s, max_tiles / 2);
             s = std::min<long long>(s, cap);
             splits = (int)std::max(1LL, s);

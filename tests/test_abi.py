@@ -113,25 +113,23 @@ def test_plan_depends_on_sm_count_only_through_the_split_heuristic(lib):
     a = plan(q, k, v, sm=152)
     b = plan(q, k, v, sm=76)
     assert a[2][0] == b[2][0] == 1
-    # decode kernel (one CTA per SM at d = 256): capped at 128 splits, which fit one wave of
-    # 152 SMs; on 76 SMs the dense-K/V planner takes the finest cap whose units fit one wave
-    # (7 of the 512 key tiles per split) and launches only those 74 splits
-    assert a[0] == 128 and b[0] == 74
+    # decode kernel (one CTA per SM at d = 256), one (tile, kv-head) pair: as many splits as
+    # fit one wave of CTAs, capped at 128 for the decode kernel (152 SMs) and 76 on 76 SMs
+    assert a[0] == 128 and b[0] == 76
     c = plan(*qkv(B=1, Sq=1, Sk=1024, Hq=8, Hkv=1, D=256, DV=256), sm=152)
     assert c[0] == 4  # 8 key tiles -> at most half as many splits
 
 
 def test_plan_128_row_kernel_split_cap(lib):
     # 128-row kernels (Sq x G > 16): at most 64 splits; both the prefill kernel (dv <= 128)
-    # and the one-tile kernel (dv > 128) take 16 positions x 8 heads per tile.  With dense
-    # K/V the heuristic's 64 splits (4 x 64 units, two waves) give way to the finest cap whose
-    # units fit one wave: 14 of the 512 key tiles per split, 37 splits, 148 units
+    # and the one-tile kernel (dv > 128) take 16 positions x 8 heads per tile.  Four (tile,
+    # kv-head) pairs: as many splits as fit one wave of 152 CTAs, 38 (no plan kernel)
     q, k, v = qkv(B=1, Sq=64, Sk=65536, Hq=8, Hkv=1, D=128, DV=128)
     s, _, grid = plan(q, k, v, sm=152)
-    assert grid[0] == 4 and s == 37
+    assert grid[0] == 4 and s == 38
     q, k, v = qkv(B=1, Sq=64, Sk=65536, Hq=8, Hkv=1, D=256, DV=256)
     s, _, grid = plan(q, k, v, sm=152)
-    assert grid[0] == 4 and s == 37
+    assert grid[0] == 4 and s == 38
     # an explicit split count is kept (the host still picks the cap: no plan kernel)
     assert plan(q, k, v, sm=152, num_splits=64)[0] == 64
 

@@ -135,8 +135,10 @@ def _model_cap(lens, Hkv, n, slots, lens_q=None, P=1):
     return best[1]
 
 
-@pytest.mark.parametrize("B,ctx,hq,hkv", [(32, 2048, 32, 8), (16, 16384, 32, 8), (64, 4096, 16, 2),
-                                           (8, 32768, 16, 2), (24, None, 16, 2)])
+# (batches with more (request, kv-head) pairs than half a wave of decode CTAs: fewer launch
+# as many splits as fit one wave, with the finest cap and no plan kernel)
+@pytest.mark.parametrize("B,ctx,hq,hkv", [(32, 2048, 32, 8), (24, 16384, 32, 8), (96, 4096, 16, 2),
+                                           (80, 32768, 16, 2), (40, None, 32, 8)])
 def test_split_cap_follows_the_key_counts(B, ctx, hq, hkv):
     """The plan kernel's cap (left in the workspace) is the model's choice for these lengths,
     and the result still matches the oracle."""
