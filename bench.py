@@ -45,10 +45,10 @@ METRIC = "FP8 attn fwd TFLOP/s (prefill) & decode HBM GB/s; % of GB300 roofline"
 # DRAM bytes (read + write) per launch from one ncu capture of each timed kernel (summaries
 # under profiles/), valid only while the kernel sources hash to the value recorded with it.
 PROFILED_TRAFFIC = {
-    "prefill": {"kernel": "prefill_kernel<128,128>", "bytes": 67.14e6,
-                "sources": ["fa8_prefill.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "7b1137eb4f864aeb"},
-    "decode": {"kernel": "decode_kernel<128,128,8>", "bytes": 2072.88e6,
-               "sources": ["fa8_decode.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "4654be073acb94db"},
+    "prefill": {"kernel": "prefill_kernel<128,128>", "bytes": 66.99e6,
+                "sources": ["fa8_prefill.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "72f1db867eccda7f"},
+    "decode": {"kernel": "decode_kernel<128,128,8>", "bytes": 2073.87e6,
+               "sources": ["fa8_decode.cuh", "fa8_kernel.cuh", "fa8_ptx.cuh"], "sha256_16": "9d0e976e12fdb2d2"},
 }
 
 
