@@ -90,8 +90,8 @@ inline cudaError_t launch_after_plan(K *kernel, const FwdParams &p, const CUtens
         return launch_after_plan(fwd_kernel<D_, DV_>, p, tq, tk, tv, grid, kNumThreads, smem, stream); \
     }
 
-// Defines launch_prefill<D, DV> (two 128-row Q tiles per CTA, dv <= 128); like
-// fwd_kernel it re-balances registers with setmaxnreg and checks the compiled count.
+// Defines launch_prefill<D, DV> (persistent, one 128-row Q tile per work unit, dv <= 128);
+// like fwd_kernel it re-balances registers with setmaxnreg and checks the compiled count.
 #define FA8_DEFINE_PREFILL(D_, DV_)                                                          \
     template <>                                                                              \
     cudaError_t launch_prefill<D_, DV_>(const FwdParams &p, const CUtensorMap &tq,           \
