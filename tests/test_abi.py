@@ -120,6 +120,68 @@ def test_plan_depends_on_sm_count_only_through_the_split_heuristic(lib):
     assert c[0] == 4  # 8 key tiles -> at most half as many splits
 
 
+def _dense_split_count(B, Sq, Sk, Hq, Hkv, D, DV, sm):
+    """The planner's split count for dense K/V and batched q, restated: the heuristic (one
+    wave of splits for few (tile, kv-head) pairs, else about eight waves), then, when the
+    launch spans more than a wave, the host-chosen cap (the plan kernel's model with the
+    one-wave candidate) and only the splits that run."""
+    import math
+    import numpy as np
+    G = Hq // Hkv
+    decode = DV % 128 == 0 and 16 % G == 0 and Sq * G <= 16
+    P = 16 // G if decode else 128 // G
+    per_sm = {(128, 128): 2}.get((D, DV), 1) if decode else 1
+    slots = per_sm * sm
+    mb = math.ceil(Sq / P)
+    base = B * mb * Hkv
+    t = math.ceil(Sk / 128)
+    max_tiles = max(1, t)
+    target = 8 * sm
+    if base >= target or max_tiles < 4:
+        return 1
+    s = slots // base if 2 * base <= slots else math.ceil(target / base)
+    s = max(1, min(s, max_tiles // 2, 128 if decode else 64))
+    if s == 1 or base * s <= slots:
+        return s
+    f32 = np.float32
+    F, BETA = f32(3.0), f32(0.4)
+    t_fine = max(2, math.ceil(t / s))
+    tiles = f32(B * t * mb)
+
+    def cost(T):
+        units = f32(B * mb * math.ceil(t / T)) * f32(Hkv)
+        tail = F + f32(min(T, t))
+        return tail if units <= f32(slots) else (F * units + tiles * f32(Hkv)) * (f32(1) / f32(slots)) + BETA * tail
+
+    best, cap = f32(3.0e38), t_fine
+    for T in [2 << c for c in range(9)] + [t_fine]:
+        if T >= t_fine and cost(T) < best:
+            best, cap = cost(T), T
+    per_split = B * mb * Hkv
+    if per_split <= slots:
+        k = slots // per_split
+        T = max(t_fine, math.ceil(t / k))
+        if cost(T) < best:
+            cap = T
+    return max(1, min(s, math.ceil(t / cap)))
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 64, 65536, 8, 1, 256, 256),     # four tile pairs: one wave of splits
+    (1, 128, 131072, 8, 1, 256, 256),   # the long-KV 128-row workload: 19 splits
+    (4, 512, 65536, 16, 2, 128, 128),   # 256 tile pairs: heuristic 5 splits, host cap
+    (2, 1000, 40000, 32, 8, 192, 128),  # ragged last tile, d = 192
+    (3, 2, 70000, 16, 2, 128, 128),     # decode kernel, two query tokens
+    (8, 1, 300000, 64, 8, 128, 128),    # decode kernel, long keys, 64 tile pairs
+    (30, 1, 9000, 32, 4, 256, 256),     # decode kernel at d = 256, 120 tile pairs
+])
+@pytest.mark.parametrize("sm", [152, 76, 148])
+def test_plan_dense_split_count_follows_the_model(lib, shape, sm):
+    B, Sq, Sk, Hq, Hkv, D, DV = shape
+    s, _, _ = plan(*qkv(B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, D=D, DV=DV), sm=sm)
+    assert s == _dense_split_count(B, Sq, Sk, Hq, Hkv, D, DV, sm)
+
+
 def test_plan_128_row_kernel_split_cap(lib):
     # 128-row kernels (Sq x G > 16): at most 64 splits; both the prefill kernel (dv <= 128)
     # and the one-tile kernel (dv > 128) take 16 positions x 8 heads per tile.  Four (tile,
