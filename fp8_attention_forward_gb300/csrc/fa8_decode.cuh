@@ -14,11 +14,12 @@
 //   S^T (128 keys x 16 rows)  = K (128 x d, K-major smem)  .  Q^T (Q: 16 x d, K-major smem)
 //   O^T (dv x 16 rows)       += V^T (V: 128 x dv smem, MN-major A operand) . P^T (16 x 128)
 //
-// so every softmax thread owns one key and holds that key's 16 scores, and the MMAs are
-// 8x smaller than a 128-row tile would make them: the kernel streams K/V at HBM rate
-// instead of spending a 128-row softmax on a handful of rows.  P^T is written to shared
-// memory MN-major (key t's 16 row bytes at 16 t, no swizzle), one 16-byte store per thread
-// and term, and read by the PV MMA from there.
+// so every softmax thread owns one key and holds that key's scores for the tile's rows (the
+// R <= 16 real ones: see decode_kernel), and the MMAs are 8x smaller than a 128-row tile
+// would make them: the kernel streams K/V at HBM rate instead of spending a 128-row softmax
+// on a handful of rows.  P^T is written to shared memory MN-major (key t's 16 row bytes at
+// 16 t, no swizzle; rows past R stay zero), one store per thread and term, and read by the
+// PV MMA from there.
 //
 // Roles (384 threads): warp 0 TMA producer, warp 1 issues the QK MMAs and warp 2 the PV
 // MMAs (two issuers, so that neither waits behind the other's barriers), warps 4-7 softmax
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
         const float dqv = p.dq ? p.dq[b * p.dq_sb + kvh * p.dq_sh] : 1.f;
         const float dkv = p.dk ? p.dk[b * p.dk_sb + kvh * p.dk_sh] : 1.f;
         const float c = p.scale_log2 * dqv * dkv;
-        // lane q < 16 keeps row q's running max (the same in every warp); every thread keeps
+        // lane q < R keeps row q's running max (the same in every warp); every thread keeps
         // the rows' P biases 8 - m (8 while m = -inf) and its key's share of the row sums
         float m_lane = -INFINITY;
         float bias[R], rsum[R];
@@ -506,7 +507,7 @@ __global__ void __launch_bounds__(kDecThreads, DecCfg<D, DV>::CTAS)
                 if (lane < R) ptx::st_shared_f32(ptx::smem_u32(alpha_s) + (uint32_t)((as * kDecRows + lane) * 4), my_alpha);
                 ptx::mbar_arrive(BAR(C::B_AF + as));
             }
-            // key t's P_hi and P_lo bytes of rows 0-15, one 16-byte store each (MN-major P^T)
+            // key t's P_hi and P_lo bytes of rows 0..R-1, one R-byte store each (MN-major P^T)
             const uint32_t phi = ptx::smem_u32(pbase) + (uint32_t)(sb * 2 * C::P_BYTES) + 16u * (uint32_t)t;
             const uint64_t c2 = ptx::f2pack(c, c);
             uint32_t hw[R / 4], lw[R / 4];
