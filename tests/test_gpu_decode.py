@@ -43,6 +43,20 @@ DECODE = [
                              descale_mode="tensor_amax", seed=307)),
     ("g8_empty_kv", dict(B=3, Hq=8, Hkv=1, D=128, DV=128, seqlens_q=[1] * 3, seqlens_k=[0, 50, 0],
                          kv_layout="varlen", causal=True, sink=True, seed=308)),
+    # tiles whose real rows (positions x q-heads per kv-head) fit in 4 or 8: the softmax and
+    # fold carry 4 or 8 rows, with one or two query positions per tile
+    ("g1_sq1_four_rows_carried", dict(B=3, Hq=2, Hkv=2, D=128, DV=128, seqlens_q=[1] * 3,
+                                      seqlens_k=[90, 1, 1100], kv_layout="paged", page_size=16,
+                                      causal=True, descale_mode="per_bkv_uniform", seed=318)),
+    ("g2_sq2_four_rows_two_positions", dict(B=2, Hq=4, Hkv=2, D=128, DV=128, seqlens_q=[2] * 2,
+                                            seqlens_k=[2, 777], kv_layout="varlen", causal=True,
+                                            sink=True, seed=319)),
+    ("g4_sq2_eight_rows_two_positions", dict(B=3, Hq=8, Hkv=2, D=128, DV=128, seqlens_q=[2] * 3,
+                                             seqlens_k=[130, 640, 1], kv_layout="paged", page_size=16,
+                                             causal=True, window_left=100, seed=320)),
+    ("g2_sq1_d256_four_rows", dict(B=2, Hq=4, Hkv=2, D=256, DV=256, seqlens_q=[1] * 2,
+                                   seqlens_k=[333, 1800], kv_layout="varlen", causal=False,
+                                   descale_mode="tensor_amax", seed=321)),
     # more than 16 rows per kv-head (4 tokens x G 8, 8 x 8, 3 x 8): the 128-row kernel in
     # both runs, with causal masking across the tokens
     ("g8_sq4_two_slots", dict(B=3, Hq=16, Hkv=2, D=128, DV=128, seqlens_q=[4] * 3,
