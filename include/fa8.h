@@ -110,7 +110,10 @@ typedef struct {
  *   the merge does not read them.  cap (2 to 512 KV tiles per split) is chosen once per
  *   call from the requests' key counts: the choice that minimises a model of the run time
  *   (a fixed cost per work unit, the units spread over the CTAs that run at once, and the
- *   longest unit's tail).
+ *   longest unit's tail).  The heuristic launches about eight waves of CTAs, or one wave
+ *   when there are few (query tile, kv-head) pairs; when every launched split fits in one
+ *   wave the finest cap is used, and with dense K/V and batched q (every length known from
+ *   the shapes) the host chooses the cap and launches only the splits that run.
  * workspace / workspace_bytes: device scratch for the split partials and the split cap the
  *   forward kernel passes to the merge kernel, at least fa8_fwd_workspace_size() bytes
  *   (may be NULL/0 when that size is 0).
